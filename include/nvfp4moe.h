@@ -1,0 +1,202 @@
+/*
+ * nvfp4moe.h - C ABI of the GB300 (sm_103a) NVFP4 mixture-of-experts layer.
+ *
+ * The layer computes, for tokens x[T,H] (bf16) and router logits[T,E] (fp32):
+ *   1. top-k routing            ids, w = topk/softmax(logits + bias)
+ *   2. permute by expert        stable sort of assignments a = t*k + j by expert
+ *   3. NVFP4 activation quant   A1 = Q(x[token(p)]) with gs_a1[e]
+ *   4. grouped FP4 GEMM gate_up C1 = alpha1_e * A1 . W13_e^T
+ *   5. SiLU-and-mul + requant   A2 = Q(silu(C1[:, gate]) * C1[:, up]) with gs_a2[e]
+ *   6. grouped FP4 GEMM down    y  = alpha2_e * A2 . W2_e^T
+ *   7. weighted combine         out[t] = sum_j w[t,j] * y[perm(t,j)] (+ shared expert row)
+ * Sources (web pages on NVFP4 MoE kernels):
+ *   - vLLM PR #29242 "[Kernel] Add NVFP4 MoE CUTLASS support for SM120": the
+ *     NVFP4 experts quant and grouped block-scaled GEMM kernels ("Purpose"),
+ *     per-expert alpha pointers with beta = 0 and per-group M, N, K in the error
+ *     text (review of nvfp4_blockwise_moe_kernel.cu), per-expert MoE offsets
+ *     (commit "Fix get_cutlass_moe_mm_data not compiling").
+ *   - FlashInfer issue #2723 "SM120 (RTX Blackwell) NVFP4 MoE: CUTLASS Grouped
+ *     Block-Scaled GEMM Produces Invalid Output ...": "Model" table (512 routed
+ *     + 1 shared expert, 10 per token, FP4 weights with FP8 block scales), "The
+ *     Problem" (grouped GEMM is the MoE expert path), "What We Tried" item 2
+ *     (FP32 block amax), "Why 39 vs 49 tok/s?" (BF16 -> FP4 per-token
+ *     activation quantization).
+ *   - unsloth "Report: NVFP4 kernel selection on SM120/SM121", SASS paragraph
+ *     under "Why it matters": E2M1 x E2M1 operands with UE4M3 scales, 4 per
+ *     64-element MMA step (one scale per 16 elements).
+ *
+ * NVFP4 data (everywhere in this ABI):
+ *   codes  : uint8, two E2M1 codes per byte, K-index 2j in bits 0-3 of byte j.
+ *   scales : uint8 E4M3 (unsigned) per 16 consecutive K elements.
+ *   gs     : float32 per-tensor (or per-expert) decode scale; value = e2m1 *
+ *            e4m3 * gs.  A block scale is E4M3(amax_block / (6 * gs)).
+ * Scale layouts (enum nvf_sf_layout):
+ *   NVF_SF_ROWMAJOR : [rows][K/16].
+ *   NVF_SF_MMA      : 512-byte atoms of 128 rows x 4 scales; atom (row/128,
+ *                     k64 = K-index/64) at byte ((row/128)*(K/64) + k64)*512,
+ *                     row r (mod 128), scale b (0..3) inside it at
+ *                     (r%32)*16 + (r/32)*4 + b.  Buffer: ceil(rows/128)*128*K/16 B.
+ *   NVF_SF_GROUPED  : rows grouped by offsets[G+1]; group g's rows form 128-row
+ *                     tiles numbered from tile_offsets[g] (exclusive prefix of
+ *                     ceil(m_g/128)); atom (tile, k64) at (tile*(K/64) + k64)*512.
+ *                     Buffer: nvfp4_grouped_scale_bytes(rows, G, K).
+ *
+ * Conventions.  All pointers marked "device" are device memory owned by the
+ * caller; the library never allocates, frees or synchronises on these paths.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ * asynchronous and reads no device data on the host.  Host-detectable errors
+ * return a status before anything is launched; launch failures return
+ * NVF_ERR_CUDA; errors detected on the device (a bounded wait that expired)
+ * are recorded in a per-device error word read by nvf_device_status().  The
+ * library never aborts, traps or prints.  Requires a compute-capability 10.3
+ * GPU (GB300); other devices get NVF_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvf_status {
+  NVF_OK = 0,
+  NVF_ERR_INVALID_ARG = 1,
+  NVF_ERR_UNSUPPORTED_DEVICE = 2,
+  NVF_ERR_WORKSPACE = 3,
+  NVF_ERR_CUDA = 4,
+  NVF_ERR_TIMEOUT = 5,
+  NVF_ERR_DEVICE_CHECK = 6
+} nvf_status;
+
+typedef enum nvf_dtype { NVF_F32 = 0, NVF_BF16 = 1 } nvf_dtype;
+typedef enum nvf_sf_layout { NVF_SF_ROWMAJOR = 0, NVF_SF_MMA = 1, NVF_SF_GROUPED = 2 } nvf_sf_layout;
+
+/* Name of a status code (static string). */
+const char* nvf_status_string(nvf_status s);
+/* Detail of the last error returned on this host thread (names the bad argument
+ * and the problem sizes); empty after a successful call. */
+const char* nvf_last_error_message(void);
+/* Version of the ABI (major * 100 + minor). */
+int32_t nvf_abi_version(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * *code = 0 if no kernel reported an error, else the kernel's error code
+ * (1..4: a pipeline wait expired in the producer / MMA / epilogue / drain);
+ * *detail = the tile or stage it happened at.  Returns NVF_ERR_TIMEOUT when a
+ * wait expired, NVF_ERR_CUDA on a CUDA error, else NVF_OK. */
+nvf_status nvf_device_status(void* stream, int32_t* code, int32_t* detail);
+
+/* Row order of prepared w13 (host helper).  The fused SiLU-and-mul epilogue
+ * needs gate and up rows of the same intermediate index side by side: row r of
+ * the prepared [2I, H] matrix is canonical row map[r], where canonical rows
+ * [0, I) are gate and [I, 2I) are up.  Blocks of 16 rows alternate: prepared
+ * rows [32c, 32c+16) = gate rows [16c, 16c+16), [32c+16, 32c+32) = up rows
+ * [16c, 16c+16).  map: host int32[2I].  I must be a positive multiple of 64. */
+nvf_status nvf_w13_row_map(int32_t I, int32_t* map);
+
+/* Bytes of an NVF_SF_GROUPED scale buffer for up to `rows` rows in G groups. */
+size_t nvfp4_grouped_scale_bytes(int64_t rows, int32_t G, int32_t K);
+
+/* Per-group global scales gs[g] = amax(x[g]) / 2688 (1 when the group is all
+ * zero): x device [groups, n] of dtype x_dtype (NVF_F32 | NVF_BF16), gs_out
+ * device float[groups].  The FP32 decode-scale reading of the pages' "FP32
+ * global scale". */
+nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, int64_t n, float* gs_out,
+                              void* stream);
+
+/* NVFP4 quantization of rows along K (step 3, and weight preparation).
+ *   x            device [*, ldx] NVF_F32 or NVF_BF16; output row p reads input
+ *                row gather_rows[p] (device int32[rows], nullable = identity).
+ *   rows, K      K a positive multiple of 64; ldx >= K, x 16-byte aligned,
+ *                ldx * element size a multiple of 16.
+ *   group_offsets device int32[G+1] (nullable): rows [offsets[g], offsets[g+1])
+ *                use gscale[g]; required for NVF_SF_GROUPED together with
+ *                tile_offsets (device int32[G+1]).  Without offsets gscale[0]
+ *                is used for every row.
+ *   gscale       device float (see above), finite and > 0.
+ *   codes        device uint8[rows, K/2] (16-byte aligned); scales: layout above.
+ * Each 16-element block: amax (FP32) -> sb = E4M3_rn_sat(amax / (6 gs)) ->
+ * r = 1 / (dec(sb) * gs) (0 if that product is 0) -> q = E2M1_rn_sat(x * r). */
+nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t K, int64_t ldx,
+                          const int32_t* gather_rows, const int32_t* group_offsets, const int32_t* tile_offsets,
+                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                          void* stream);
+
+/* Top-k routing and permutation (steps 1-2).
+ *   logits       device float[T, E]; bias device float[E] or NULL, added in FP32.
+ *   T >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32); renormalize: softmax over
+ *   the k selected logits (1) or over all E (0); shared_expert 0|1 adds expert
+ *   id E seen by every token with weight 1 (its rows follow all routed rows).
+ * Outputs (device): topk_ids int32[T,k] (descending logit, ties -> lower id),
+ *   topk_w float[T,k], expert_offsets int32[E'+1] (E' = E + shared),
+ *   tile_offsets int32[E'+1] (prefix of ceil(m_e/128)), perm_to_src int32[R],
+ *   src_to_perm int32[R], perm_token int32[R] (R = T*k + shared*T; assignment
+ *   a = t*k + j, shared rows a = T*k + t).
+ *   ws / ws_bytes: device scratch of at least moe_route_permute_workspace_size(). */
+nvf_status moe_route_permute_workspace_size(int32_t T, int32_t E, size_t* bytes);
+nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k,
+                             int32_t renormalize, int32_t shared_expert, int32_t* topk_ids, float* topk_w,
+                             int32_t* expert_offsets, int32_t* tile_offsets, int32_t* perm_to_src,
+                             int32_t* src_to_perm, int32_t* perm_token, void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped block-scaled FP4 GEMM (steps 4 / 6 with a plain epilogue):
+ *   D[row, n] = gs_a[g] * gs_b[g] * sum_k A[row, k] B[g, n, k]   for offsets[g] <= row < offsets[g+1].
+ *   A       device uint8[a_rows, K/2] codes; a_rows bounds every row the GEMM may
+ *           touch (offsets[G] <= a_rows); A_sf NVF_SF_GROUPED scales.
+ *   B       device uint8[G, N, K/2]; B_sf NVF_SF_MMA scales of the [G*N, K] matrix.
+ *   gs_a, gs_b device float[G]; group_offsets, tile_offsets device int32[G+1].
+ *   N a positive multiple of 128, K a positive multiple of 64, K/2 a multiple of 16.
+ *   D       device [a_rows, ldd] of out_dtype (NVF_F32 | NVF_BF16); only rows of
+ *           groups are written.  ldd * element size a multiple of 16. */
+nvf_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
+                              const uint8_t* B_sf, const float* gs_a, const float* gs_b, const int32_t* group_offsets,
+                              const int32_t* tile_offsets, int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D,
+                              int64_t ldd, void* stream);
+
+/* Prepared expert weights (all device pointers). */
+typedef struct nvf_moe_weights {
+  int32_t E;               /* routed experts */
+  int32_t H, I;            /* hidden, intermediate: multiples of 128 and 64 */
+  int32_t shared;          /* 1: expert E is an always-on shared expert */
+  const uint8_t* w13;      /* uint8[E', 2I, H/2], rows in nvf_w13_row_map order */
+  const uint8_t* w13_sf;   /* NVF_SF_MMA scales of [E'*2I, H] */
+  const float* gs_w13;     /* float[E'] */
+  const uint8_t* w2;       /* uint8[E', H, I/2] */
+  const uint8_t* w2_sf;    /* NVF_SF_MMA scales of [E'*H, I] */
+  const float* gs_w2;      /* float[E'] */
+} nvf_moe_weights;
+
+/* Byte offsets of the forward pass' intermediates inside its workspace
+ * (debug and test access; layouts as documented above). */
+typedef struct nvf_moe_ws_layout {
+  size_t topk_ids, topk_w, expert_offsets, tile_offsets, perm_to_src, src_to_perm, perm_token;
+  size_t a1_codes, a1_sf, a2_codes, a2_sf, y;  /* y: float[R, H] */
+  size_t route_scratch, total;
+  int64_t R;                                   /* rows after permutation */
+} nvf_moe_ws_layout;
+
+nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I, int32_t k, int32_t shared,
+                                      nvf_moe_ws_layout* layout);
+
+/* The whole layer (steps 1-7) on one stream.
+ *   x        device bf16[T, H]; logits device float[T, E]; bias NULL or float[E].
+ *   gs_a1, gs_a2 device float[E']: static activation global scales.
+ *   out      device [T, H] of out_dtype (NVF_F32 | NVF_BF16).
+ *   h_dump   NULL, or device float[R, I] receiving silu(gate) * up (row = perm slot).
+ *   ws       device scratch of nvfp4_moe_workspace_layout().total bytes, 256-byte aligned.
+ *   stage_events NULL, or NVF_MOE_STAGE_EVENTS cudaEvent_t handles recorded on `stream`
+ *            before routing and after each stage (route+permute, activation quant,
+ *            gate_up GEMM, down GEMM, combine), for per-stage timing. */
+#define NVF_MOE_STAGE_EVENTS 6
+nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
+                             int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,
+                             int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
+                             void* const* stage_events, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,275 @@
+"""Python binding of libnvfp4moe, the sm_103a NVFP4 mixture-of-experts layer.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+behind the C ABI declared in include/nvfp4moe.h.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing or the device is not a GB300 (compute capability 10.3), calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
+
+NVF_F32, NVF_BF16 = 0, 1
+SF_ROWMAJOR, SF_MMA, SF_GROUPED = 0, 1, 2
+STATUS = {0: "NVF_OK", 1: "NVF_ERR_INVALID_ARG", 2: "NVF_ERR_UNSUPPORTED_DEVICE", 3: "NVF_ERR_WORKSPACE",
+          4: "NVF_ERR_CUDA", 5: "NVF_ERR_TIMEOUT", 6: "NVF_ERR_DEVICE_CHECK"}
+
+# Every entry point declared in include/nvfp4moe.h, with its ctypes signature.
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "nvf_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nvf_last_error_message": (ctypes.c_char_p, []),
+    "nvf_abi_version": (_I32, []),
+    "nvf_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "nvf_w13_row_map": (ctypes.c_int, [_I32, ctypes.POINTER(_I32)]),
+    "nvfp4_grouped_scale_bytes": (_SZ, [_I64, _I32, _I32]),
+    "nvfp4_global_scale": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
+    "nvfp4_quantize": (ctypes.c_int, [_P, _I32, _I64, _I32, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _P]),
+    "moe_route_permute_workspace_size": (ctypes.c_int, [_I32, _I32, ctypes.POINTER(_SZ)]),
+    "moe_route_permute": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                         _SZ, _P]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
+                                          _P]),
+    "nvfp4_moe_workspace_layout": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
+    "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
+                                         _P]),
+}
+
+
+class NvfError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class MoEWeightsC(ctypes.Structure):
+    _fields_ = [("E", _I32), ("H", _I32), ("I", _I32), ("shared", _I32), ("w13", _P), ("w13_sf", _P),
+                ("gs_w13", _P), ("w2", _P), ("w2_sf", _P), ("gs_w2", _P)]
+
+
+class WorkspaceLayoutC(ctypes.Structure):
+    _fields_ = [(n, _SZ) for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src",
+                                    "src_to_perm", "perm_token", "a1_codes", "a1_sf", "a2_codes", "a2_sf", "y",
+                                    "route_scratch", "total")] + [("R", _I64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m nvfp4_moe_grouped_router_gb300.build`"
+                              " (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise NvfError(status, lib().nvf_last_error_message().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return NVF_F32
+    if t.dtype == torch.bfloat16:
+        return NVF_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+# ----------------------------------------------------------------------------- small helpers
+def device_status():
+    """(code, detail) of the current device's error word (synchronises the stream, then clears it)."""
+    code, detail = _I32(0), _I32(0)
+    st = lib().nvf_device_status(_stream(), ctypes.byref(code), ctypes.byref(detail))
+    if st not in (0, 5):
+        _check(st)
+    return code.value, detail.value
+
+
+def w13_row_map(I: int):
+    m = (_I32 * (2 * I))()
+    _check(lib().nvf_w13_row_map(I, m))
+    return list(m)
+
+
+def grouped_scale_bytes(rows: int, G: int, K: int) -> int:
+    return int(lib().nvfp4_grouped_scale_bytes(rows, G, K))
+
+
+def mma_scale_bytes(rows: int, K: int) -> int:
+    return (rows + 127) // 128 * 128 * (K // 16)
+
+
+# ----------------------------------------------------------------------------- entry points
+def global_scale(x: torch.Tensor, groups: int = 1) -> torch.Tensor:
+    """gs[g] = amax(x[g]) / 2688 for x viewed as [groups, n]."""
+    _cuda(x, "x")
+    gs = torch.empty(groups, dtype=torch.float32, device=x.device)
+    _check(lib().nvfp4_global_scale(_ptr(x), _dtype_code(x), groups, x.numel() // groups, _ptr(gs), _stream()))
+    return gs
+
+
+def quantize(x: torch.Tensor, gscale: torch.Tensor, layout: int = SF_ROWMAJOR, gather=None, offsets=None,
+             tile_offsets=None, rows=None, codes=None, scales=None):
+    """NVFP4 codes [rows, K/2] and scales (layout) of the rows of a 2-D tensor x."""
+    _cuda(x, "x")
+    K = x.shape[1]
+    rows = (gather.numel() if gather is not None else x.shape[0]) if rows is None else rows
+    G = offsets.numel() - 1 if offsets is not None else 1
+    if codes is None:
+        codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        n = {SF_ROWMAJOR: rows * (K // 16), SF_MMA: mma_scale_bytes(rows, K),
+             SF_GROUPED: grouped_scale_bytes(rows, G, K)}[layout]
+        scales = torch.zeros(max(n, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().nvfp4_quantize(_ptr(x), _dtype_code(x), rows, K, x.stride(0), _ptr(gather), _ptr(offsets),
+                                _ptr(tile_offsets), G, _ptr(gscale), _ptr(codes), _ptr(scales), layout, _stream()))
+    return codes, scales
+
+
+def route_permute(logits: torch.Tensor, k: int, bias=None, renormalize=True, shared=False):
+    _cuda(logits, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    R = T * k + (T if shared else 0)
+    Et = E + int(shared)
+    out = dict(topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+               topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+               expert_offsets=torch.empty(Et + 1, dtype=torch.int32, device=dev),
+               tile_offsets=torch.empty(Et + 1, dtype=torch.int32, device=dev),
+               perm_to_src=torch.empty(R, dtype=torch.int32, device=dev),
+               src_to_perm=torch.empty(R, dtype=torch.int32, device=dev),
+               perm_token=torch.empty(R, dtype=torch.int32, device=dev))
+    nbytes = _SZ(0)
+    _check(lib().moe_route_permute_workspace_size(T, E, ctypes.byref(nbytes)))
+    ws = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+    o = out
+    _check(lib().moe_route_permute(_ptr(logits), _ptr(bias), T, E, k, int(renormalize), int(shared),
+                                   _ptr(o["topk_ids"]), _ptr(o["topk_w"]), _ptr(o["expert_offsets"]),
+                                   _ptr(o["tile_offsets"]), _ptr(o["perm_to_src"]), _ptr(o["src_to_perm"]),
+                                   _ptr(o["perm_token"]), _ptr(ws), nbytes.value, _stream()))
+    return out
+
+
+def grouped_gemm(A, A_sf, B, B_sf, gs_a, gs_b, offsets, tile_offsets, N: int, K: int, out_dtype=torch.float32,
+                 D=None):
+    """D[row] = gs_a[g] gs_b[g] A[row] . B[g]^T for the rows of group g (rows of A beyond offsets[G] untouched)."""
+    a_rows = A.shape[0]
+    G = offsets.numel() - 1
+    if D is None:
+        D = torch.zeros(a_rows, N, dtype=out_dtype, device=A.device)
+    code = NVF_F32 if D.dtype == torch.float32 else NVF_BF16
+    _check(lib().nvfp4_grouped_gemm(_ptr(A), _ptr(A_sf), a_rows, _ptr(B), _ptr(B_sf), _ptr(gs_a), _ptr(gs_b),
+                                    _ptr(offsets), _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0),
+                                    _stream()))
+    return D
+
+
+# ----------------------------------------------------------------------------- the layer
+@dataclass
+class MoEWeights:
+    E: int
+    H: int
+    I: int
+    shared: bool
+    w13: torch.Tensor     # uint8 [E', 2I, H/2], prepared row order
+    w13_sf: torch.Tensor  # MMA-layout scales
+    gs_w13: torch.Tensor  # float [E']
+    w2: torch.Tensor      # uint8 [E', H, I/2]
+    w2_sf: torch.Tensor
+    gs_w2: torch.Tensor
+
+    def c_struct(self) -> MoEWeightsC:
+        return MoEWeightsC(self.E, self.H, self.I, int(self.shared), self.w13.data_ptr(), self.w13_sf.data_ptr(),
+                           self.gs_w13.data_ptr(), self.w2.data_ptr(), self.w2_sf.data_ptr(),
+                           self.gs_w2.data_ptr())
+
+
+def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="cuda") -> MoEWeights:
+    """Quantize FP32 expert weights on the device into the layer's layout.
+
+    expert_fp32(e) -> (w13 [2I, H], w2 [H, I]) float32 tensors on `device` (gate rows
+    first, then up rows).  Per expert: gs = amax / 2688, NVFP4 rows along the
+    input dimension, w13 rows reordered by w13_row_map, scales in MMA layout.
+    """
+    Et = E + int(shared)
+    w13 = torch.empty(Et, 2 * I, H // 2, dtype=torch.uint8, device=device)
+    w13_sf = torch.empty(Et * 2 * I * H // 16, dtype=torch.uint8, device=device)
+    w2 = torch.empty(Et, H, I // 2, dtype=torch.uint8, device=device)
+    w2_sf = torch.empty(Et * H * I // 16, dtype=torch.uint8, device=device)
+    gs13 = torch.empty(Et, dtype=torch.float32, device=device)
+    gs2 = torch.empty(Et, dtype=torch.float32, device=device)
+    rmap = torch.tensor(w13_row_map(I), dtype=torch.int32, device=device)
+    n13, n2 = 2 * I * H // 16, H * I // 16
+    for e in range(Et):
+        a, b = expert_fp32(e)
+        a = a.to(device=device, dtype=torch.float32).contiguous()
+        b = b.to(device=device, dtype=torch.float32).contiguous()
+        g13 = global_scale(a)
+        g2 = global_scale(b)
+        gs13[e:e + 1].copy_(g13)
+        gs2[e:e + 1].copy_(g2)
+        quantize(a, g13, SF_MMA, gather=rmap, codes=w13[e], scales=w13_sf[e * n13:(e + 1) * n13])
+        quantize(b, g2, SF_MMA, codes=w2[e], scales=w2_sf[e * n2:(e + 1) * n2])
+    return MoEWeights(E, H, I, shared, w13, w13_sf, gs13, w2, w2_sf, gs2)
+
+
+def workspace_layout(T: int, E: int, H: int, I: int, k: int, shared: bool) -> dict:
+    L = WorkspaceLayoutC()
+    _check(lib().nvfp4_moe_workspace_layout(T, E, H, I, k, int(shared), ctypes.byref(L)))
+    return {n: getattr(L, n) for n, _ in L._fields_}
+
+
+def workspace(T: int, w: MoEWeights, k: int) -> torch.Tensor:
+    n = workspace_layout(T, w.E, w.H, w.I, k, w.shared)["total"]
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=w.w13.device)
+
+
+def moe_forward(w: MoEWeights, x, logits, k: int, gs_a1, gs_a2, bias=None, renormalize=True,
+                out_dtype=torch.float32, out=None, h_dump=None, ws=None, stage_events=None, cw=None):
+    """The whole layer: route, permute, quantize, gate_up GEMM + SiLU*up requant, down GEMM, combine."""
+    _cuda(x, "x")
+    _cuda(logits, "logits")
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, w.H, dtype=out_dtype, device=x.device)
+    if ws is None:
+        ws = workspace(T, w, k)
+    cw = w.c_struct() if cw is None else cw
+    ev = None
+    if stage_events is not None:
+        ev = (ctypes.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+    _check(lib().nvfp4_moe_forward(ctypes.byref(cw), _ptr(x), _ptr(logits), _ptr(bias), T, k, int(renormalize),
+                                   _ptr(gs_a1), _ptr(gs_a2), NVF_F32 if out.dtype == torch.float32 else NVF_BF16,
+                                   _ptr(out), _ptr(h_dump), _ptr(ws), ws.numel(), ev, _stream()))
+    return out

@@ -1,0 +1,387 @@
+// C ABI of the NVFP4 MoE layer: argument validation, workspace carving and the
+// launch sequence.  See include/nvfp4moe.h for the contract of every entry point.
+#include "../../include/nvfp4moe.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace nvf {
+
+__device__ int g_device_error[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local char g_msg[512];
+
+nvf_status fail(nvf_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+nvf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(NVF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 ok, -1 unsupported
+  int sms = 0;
+  int* err = nullptr;
+  int major = 0, minor = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Validates the current device once (CC 10.3) and caches its SM count and the
+// address of its error word.
+nvf_status current_device(DeviceInfo** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (d < 0 || d >= kMaxDevices) return fail(NVF_ERR_UNSUPPORTED_DEVICE, "device ordinal %d out of range", d);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[d];
+  if (di.checked == 0) {
+    cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, d);
+    cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, d);
+    cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d);
+    if (di.major != 10 || di.minor != 3) {
+      di.checked = -1;
+    } else {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_device_error);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+      di.err = static_cast<int*>(p);
+      di.checked = 1;
+    }
+  }
+  if (di.checked < 0)
+    return fail(NVF_ERR_UNSUPPORTED_DEVICE, "device %d has compute capability %d.%d; this library is built for 10.3 (GB300)",
+                d, di.major, di.minor);
+  *out = &di;
+  return NVF_OK;
+}
+
+thread_local int g_cur_sms = 148;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+int sm_count() { return g_cur_sms; }
+int* device_error_word() {
+  DeviceInfo* di = nullptr;
+  return current_device(&di) == NVF_OK ? di->err : nullptr;
+}
+
+}  // namespace nvf
+
+using namespace nvf;
+
+#define NVF_BEGIN()                                 \
+  g_msg[0] = 0;                                     \
+  DeviceInfo* dev_ = nullptr;                       \
+  {                                                 \
+    nvf_status st_ = current_device(&dev_);         \
+    if (st_ != NVF_OK) return st_;                  \
+    g_cur_sms = dev_->sms;                          \
+  }
+#define NVF_REQUIRE(cond, ...) \
+  do {                         \
+    if (!(cond)) return fail(NVF_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+#define NVF_CUDA(call, what)                       \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+extern "C" {
+
+const char* nvf_status_string(nvf_status s) {
+  switch (s) {
+    case NVF_OK: return "NVF_OK";
+    case NVF_ERR_INVALID_ARG: return "NVF_ERR_INVALID_ARG";
+    case NVF_ERR_UNSUPPORTED_DEVICE: return "NVF_ERR_UNSUPPORTED_DEVICE";
+    case NVF_ERR_WORKSPACE: return "NVF_ERR_WORKSPACE";
+    case NVF_ERR_CUDA: return "NVF_ERR_CUDA";
+    case NVF_ERR_TIMEOUT: return "NVF_ERR_TIMEOUT";
+    case NVF_ERR_DEVICE_CHECK: return "NVF_ERR_DEVICE_CHECK";
+  }
+  return "NVF_ERR_UNKNOWN";
+}
+
+const char* nvf_last_error_message(void) { return g_msg; }
+
+int32_t nvf_abi_version(void) { return 100; }
+
+nvf_status nvf_device_status(void* stream, int32_t* code, int32_t* detail) {
+  NVF_BEGIN();
+  NVF_REQUIRE(code != nullptr, "code must not be NULL");
+  NVF_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  int h[2] = {0, 0};
+  NVF_CUDA(cudaMemcpy(h, dev_->err, sizeof(h), cudaMemcpyDeviceToHost), "read error word");
+  NVF_CUDA(cudaMemset(dev_->err, 0, sizeof(h)), "clear error word");
+  *code = h[0];
+  if (detail) *detail = h[1];
+  if (h[0] == 0) return NVF_OK;
+  return fail(NVF_ERR_TIMEOUT, "a kernel pipeline wait expired (code %d, at %d)", h[0], h[1]);
+}
+
+nvf_status nvf_w13_row_map(int32_t I, int32_t* map) {
+  g_msg[0] = 0;
+  NVF_REQUIRE(I > 0 && I % 64 == 0, "I=%d must be a positive multiple of 64", I);
+  NVF_REQUIRE(map != nullptr, "map must not be NULL");
+  for (int32_t r = 0; r < 2 * I; ++r) {
+    const int32_t c = r / 32, within = r % 32;
+    map[r] = within < 16 ? 16 * c + within : I + 16 * c + (within - 16);
+  }
+  return NVF_OK;
+}
+
+size_t nvfp4_grouped_scale_bytes(int64_t rows, int32_t G, int32_t K) {
+  if (rows < 0 || G < 0 || K <= 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128 + G) * 128 * static_cast<size_t>(K / 16);
+}
+
+nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, int64_t n, float* gs_out,
+                              void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(x != nullptr && gs_out != nullptr, "x and gs_out must not be NULL");
+  NVF_REQUIRE(x_dtype == NVF_F32 || x_dtype == NVF_BF16, "x_dtype=%d must be NVF_F32 or NVF_BF16", x_dtype);
+  NVF_REQUIRE(groups >= 1 && groups <= 65535 && n >= 1, "groups=%lld (1..65535), n=%lld (>=1)", (long long)groups,
+              (long long)n);
+  NVF_CUDA(launch_global_scale(x, x_dtype, groups, n, gs_out, static_cast<cudaStream_t>(stream)), "global scale");
+  return NVF_OK;
+}
+
+nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t K, int64_t ldx,
+                          const int32_t* gather_rows, const int32_t* group_offsets, const int32_t* tile_offsets,
+                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                          void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(x && gscale && codes && scales, "x, gscale, codes and scales must not be NULL");
+  NVF_REQUIRE(x_dtype == NVF_F32 || x_dtype == NVF_BF16, "x_dtype=%d must be NVF_F32 or NVF_BF16", x_dtype);
+  NVF_REQUIRE(rows >= 0 && K > 0 && K % 64 == 0, "rows=%lld K=%d: K must be a positive multiple of 64",
+              (long long)rows, K);
+  NVF_REQUIRE(ldx >= K, "ldx=%lld < K=%d", (long long)ldx, K);
+  const int esz = x_dtype == NVF_F32 ? 4 : 2;
+  NVF_REQUIRE(aligned16(x) && (ldx * esz) % 16 == 0, "x must be 16-byte aligned with a 16-byte multiple row pitch");
+  NVF_REQUIRE(aligned16(codes) && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0,
+              "codes must be 16-byte and scales 4-byte aligned");
+  NVF_REQUIRE(scale_layout >= NVF_SF_ROWMAJOR && scale_layout <= NVF_SF_GROUPED, "bad scale_layout %d", scale_layout);
+  if (group_offsets) NVF_REQUIRE(G >= 1, "G=%d must be >= 1 with group_offsets", G);
+  if (scale_layout == NVF_SF_GROUPED)
+    NVF_REQUIRE(group_offsets && tile_offsets, "NVF_SF_GROUPED needs group_offsets and tile_offsets");
+  QuantArgs a{x, x_dtype, rows, K, ldx, gather_rows, group_offsets, tile_offsets, group_offsets ? G : 1,
+              gscale, codes, scales, scale_layout};
+  NVF_CUDA(launch_quantize(a, static_cast<cudaStream_t>(stream)), "quantize launch");
+  return NVF_OK;
+}
+
+nvf_status moe_route_permute_workspace_size(int32_t T, int32_t E, size_t* bytes) {
+  g_msg[0] = 0;
+  NVF_REQUIRE(bytes != nullptr && T >= 0 && E >= 1, "bad arguments");
+  *bytes = align256(2 * static_cast<size_t>(route_num_chunks(T)) * E * sizeof(int32_t));
+  if (*bytes == 0) *bytes = 256;
+  return NVF_OK;
+}
+
+static nvf_status validate_route(int32_t T, int32_t E, int32_t k, int32_t shared) {
+  NVF_REQUIRE(T >= 0 && T <= (1 << 24), "T=%d must be in [0, 2^24]", T);
+  NVF_REQUIRE(E >= 1 && E <= 1024, "E=%d must be in [1, 1024]", E);
+  NVF_REQUIRE(k >= 1 && k <= E && k <= 32, "k=%d must be in [1, min(E=%d, 32)]", k, E);
+  NVF_REQUIRE(shared == 0 || shared == 1, "shared_expert=%d must be 0 or 1", shared);
+  NVF_REQUIRE(static_cast<int64_t>(T) * (k + shared) < (int64_t(1) << 31), "T*(k+shared) overflows int32");
+  return NVF_OK;
+}
+
+nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k,
+                             int32_t renormalize, int32_t shared_expert, int32_t* topk_ids, float* topk_w,
+                             int32_t* expert_offsets, int32_t* tile_offsets, int32_t* perm_to_src,
+                             int32_t* src_to_perm, int32_t* perm_token, void* ws, size_t ws_bytes, void* stream) {
+  NVF_BEGIN();
+  {
+    nvf_status s = validate_route(T, E, k, shared_expert);
+    if (s != NVF_OK) return s;
+  }
+  NVF_REQUIRE(expert_offsets && tile_offsets, "expert_offsets and tile_offsets must not be NULL");
+  if (T > 0)
+    NVF_REQUIRE(logits && topk_ids && topk_w && perm_to_src && src_to_perm && perm_token,
+                "logits, topk_ids, topk_w, perm_to_src, src_to_perm and perm_token must not be NULL");
+  size_t need = 0;
+  moe_route_permute_workspace_size(T, E, &need);
+  NVF_REQUIRE(ws != nullptr || need == 0, "ws must not be NULL");
+  if (ws_bytes < need) return fail(NVF_ERR_WORKSPACE, "workspace %zu bytes < %zu needed (T=%d E=%d)", ws_bytes, need, T, E);
+  const int nch = route_num_chunks(T);
+  RouteArgs a{logits, bias, T, E, k, renormalize ? 1 : 0, shared_expert, topk_ids, topk_w, expert_offsets,
+              tile_offsets, perm_to_src, src_to_perm, perm_token, static_cast<int32_t*>(ws),
+              static_cast<int32_t*>(ws) + static_cast<size_t>(nch) * E};
+  NVF_CUDA(launch_route(a, static_cast<cudaStream_t>(stream)), "route launch");
+  return NVF_OK;
+}
+
+static nvf_status validate_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
+                                const uint8_t* B_sf, int32_t G, int32_t N, int32_t K) {
+  NVF_REQUIRE(A && A_sf && B && B_sf, "A, A_sf, B and B_sf must not be NULL");
+  NVF_REQUIRE(G >= 1 && G <= 4096, "G=%d must be in [1, 4096]", G);
+  NVF_REQUIRE(N > 0 && N % 128 == 0, "N=%d must be a positive multiple of 128", N);
+  NVF_REQUIRE(K > 0 && K % 64 == 0, "K=%d must be a positive multiple of 64", K);
+  NVF_REQUIRE(a_rows >= 0 && a_rows < (int64_t(1) << 31), "a_rows=%lld out of range", (long long)a_rows);
+  NVF_REQUIRE(static_cast<int64_t>(G) * N < (int64_t(1) << 31), "G*N overflows int32");
+  NVF_REQUIRE(aligned16(A) && aligned16(B) && aligned16(A_sf) && aligned16(B_sf),
+              "A, B, A_sf and B_sf must be 16-byte aligned");
+  return NVF_OK;
+}
+
+nvf_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
+                              const uint8_t* B_sf, const float* gs_a, const float* gs_b, const int32_t* group_offsets,
+                              const int32_t* tile_offsets, int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D,
+                              int64_t ldd, void* stream) {
+  NVF_BEGIN();
+  {
+    nvf_status s = validate_gemm(A, A_sf, a_rows, B, B_sf, G, N, K);
+    if (s != NVF_OK) return s;
+  }
+  NVF_REQUIRE(gs_a && gs_b && group_offsets && tile_offsets && D, "gs_a, gs_b, offsets and D must not be NULL");
+  NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
+  const int esz = out_dtype == NVF_F32 ? 4 : 2;
+  NVF_REQUIRE(ldd >= N && (ldd * esz) % 16 == 0 && aligned16(D),
+              "D must be 16-byte aligned with ldd >= N=%d and ldd*%d bytes a multiple of 16 (ldd=%lld)", N, esz,
+              (long long)ldd);
+  GemmArgs a{};
+  a.a = A; a.a_rows = a_rows; a.a_sf = A_sf; a.b = B; a.b_sf = B_sf; a.gs_a = gs_a; a.gs_b = gs_b;
+  a.offsets = group_offsets; a.tile_offs = tile_offsets; a.G = G; a.N = N; a.K = K;
+  a.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
+  a.d = D; a.ldd = ldd; a.err = dev_->err;
+  const char* why = nullptr;
+  cudaError_t e = launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess)
+    return fail(NVF_ERR_CUDA, "grouped GEMM (G=%d M<=%lld N=%d K=%d): %s", G, (long long)a_rows, N, K,
+                why ? why : cudaGetErrorString(e));
+  return NVF_OK;
+}
+
+nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I, int32_t k, int32_t shared,
+                                      nvf_moe_ws_layout* L) {
+  g_msg[0] = 0;
+  NVF_REQUIRE(L != nullptr, "layout must not be NULL");
+  {
+    nvf_status s = validate_route(T, E, k, shared);
+    if (s != NVF_OK) return s;
+  }
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(I > 0 && I % 64 == 0, "I=%d must be a positive multiple of 64", I);
+  const int64_t Et = E + shared;
+  const int64_t R = static_cast<int64_t>(T) * k + (shared ? T : 0);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L->R = R;
+  L->topk_ids = take(sizeof(int32_t) * T * k);
+  L->topk_w = take(sizeof(float) * T * k);
+  L->expert_offsets = take(sizeof(int32_t) * (Et + 1));
+  L->tile_offsets = take(sizeof(int32_t) * (Et + 1));
+  L->perm_to_src = take(sizeof(int32_t) * R);
+  L->src_to_perm = take(sizeof(int32_t) * R);
+  L->perm_token = take(sizeof(int32_t) * R);
+  size_t rs = 0;
+  moe_route_permute_workspace_size(T, E, &rs);
+  L->route_scratch = take(rs);
+  L->a1_codes = take(static_cast<size_t>(R) * H / 2);
+  L->a1_sf = take(nvfp4_grouped_scale_bytes(R, static_cast<int32_t>(Et), H));
+  L->a2_codes = take(static_cast<size_t>(R) * I / 2);
+  L->a2_sf = take(nvfp4_grouped_scale_bytes(R, static_cast<int32_t>(Et), I));
+  L->y = take(sizeof(float) * static_cast<size_t>(R) * H);
+  L->total = off;
+  return NVF_OK;
+}
+
+nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
+                             int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,
+                             int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
+                             void* const* stage_events, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(w != nullptr, "weights must not be NULL");
+  nvf_moe_ws_layout L;
+  {
+    nvf_status s = nvfp4_moe_workspace_layout(T, w->E, w->H, w->I, k, w->shared, &L);
+    if (s != NVF_OK) return s;
+  }
+  const int32_t E = w->E, H = w->H, I = w->I, Et = w->E + w->shared;
+  NVF_REQUIRE(w->w13 && w->w13_sf && w->gs_w13 && w->w2 && w->w2_sf && w->gs_w2, "weight pointers must not be NULL");
+  NVF_REQUIRE(aligned16(w->w13) && aligned16(w->w2) && aligned16(w->w13_sf) && aligned16(w->w2_sf),
+              "weight buffers must be 16-byte aligned");
+  NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
+  if (T == 0) return NVF_OK;
+  NVF_REQUIRE(x && logits && gs_a1 && gs_a2 && out, "x, logits, gs_a1, gs_a2 and out must not be NULL");
+  NVF_REQUIRE(aligned16(x) && aligned16(out) && (h_dump == nullptr || aligned16(h_dump)),
+              "x, out and h_dump must be 16-byte aligned");
+  NVF_REQUIRE(ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "ws must be 256-byte aligned");
+  if (ws_bytes < L.total)
+    return fail(NVF_ERR_WORKSPACE, "workspace %zu bytes < %zu needed (T=%d E=%d H=%d I=%d k=%d)", ws_bytes, L.total,
+                T, E, H, I, k);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto i32 = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
+  const int nch = route_num_chunks(T);
+  auto mark = [&](int i) -> cudaError_t {
+    return stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) : cudaSuccess;
+  };
+  NVF_CUDA(mark(0), "cudaEventRecord");
+
+  RouteArgs ra{logits, bias, T, E, k, renormalize ? 1 : 0, w->shared, i32(L.topk_ids),
+               reinterpret_cast<float*>(base + L.topk_w), i32(L.expert_offsets), i32(L.tile_offsets),
+               i32(L.perm_to_src), i32(L.src_to_perm), i32(L.perm_token), i32(L.route_scratch),
+               i32(L.route_scratch) + static_cast<size_t>(nch) * E};
+  NVF_CUDA(launch_route(ra, s), "route launch");
+  NVF_CUDA(mark(1), "cudaEventRecord");
+
+  QuantArgs qa{x, NVF_BF16, L.R, H, H, i32(L.perm_token), i32(L.expert_offsets), i32(L.tile_offsets), Et,
+               gs_a1, base + L.a1_codes, base + L.a1_sf, NVF_SF_GROUPED};
+  NVF_CUDA(launch_quantize(qa, s), "activation quantize launch");
+  NVF_CUDA(mark(2), "cudaEventRecord");
+
+  const char* why = nullptr;
+  GemmArgs g1{};
+  g1.a = base + L.a1_codes; g1.a_rows = L.R; g1.a_sf = base + L.a1_sf;
+  g1.b = w->w13; g1.b_sf = w->w13_sf; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
+  g1.offsets = i32(L.expert_offsets); g1.tile_offs = i32(L.tile_offsets); g1.G = Et; g1.N = 2 * I; g1.K = H;
+  g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2_codes; g1.q_sf = base + L.a2_sf; g1.gs_q = gs_a2;
+  g1.h_dump = h_dump; g1.err = dev_->err;
+  cudaError_t e = launch_grouped_gemm(g1, s, &why);
+  if (e != cudaSuccess)
+    return fail(NVF_ERR_CUDA, "gate_up GEMM (E'=%d R=%lld N=%d K=%d): %s", Et, (long long)L.R, 2 * I, H,
+                why ? why : cudaGetErrorString(e));
+  NVF_CUDA(mark(3), "cudaEventRecord");
+
+  GemmArgs g2{};
+  g2.a = base + L.a2_codes; g2.a_rows = L.R; g2.a_sf = base + L.a2_sf;
+  g2.b = w->w2; g2.b_sf = w->w2_sf; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
+  g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
+  g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
+  e = launch_grouped_gemm(g2, s, &why);
+  if (e != cudaSuccess)
+    return fail(NVF_ERR_CUDA, "down GEMM (E'=%d R=%lld N=%d K=%d): %s", Et, (long long)L.R, H, I,
+                why ? why : cudaGetErrorString(e));
+  NVF_CUDA(mark(4), "cudaEventRecord");
+
+  NVF_CUDA(launch_combine(reinterpret_cast<const float*>(base + L.y), H, reinterpret_cast<const float*>(base + L.topk_w),
+                          i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s),
+           "combine launch");
+  NVF_CUDA(mark(5), "cudaEventRecord");
+  return NVF_OK;
+}
+
+}  // extern "C"

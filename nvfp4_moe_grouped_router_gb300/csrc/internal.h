@@ -1,0 +1,80 @@
+// Host-side launchers shared between the kernel translation units and the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nvf {
+
+enum XDtype : int { X_F32 = 0, X_BF16 = 1 };
+
+struct QuantArgs {
+  const void* x;            // [src_rows, ldx] f32 or bf16
+  int x_dtype;
+  int64_t rows;             // output rows
+  int32_t K;                // multiple of 64
+  int64_t ldx;              // elements
+  const int32_t* gather;    // nullable [rows]: output row p reads x row gather[p]
+  const int32_t* offsets;   // nullable [G+1]: row groups (per-group global scale, grouped layout)
+  const int32_t* tile_offs; // [G+1], grouped layout only
+  int32_t G;
+  const float* gs;          // [G] when offsets given, else [1]
+  uint8_t* codes;           // [rows, K/2]
+  uint8_t* scales;          // per layout
+  int layout;
+};
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
+cudaError_t launch_global_scale(const void* x, int x_dtype, int64_t groups, int64_t n_per_group, float* gs_out,
+                                cudaStream_t s);
+
+struct RouteArgs {
+  const float* logits;      // [T, E]
+  const float* bias;        // nullable [E]
+  int32_t T, E, k, renormalize, shared;
+  int32_t* ids;             // [T, k]
+  float* weights;           // [T, k]
+  int32_t* offsets;         // [E'+1]
+  int32_t* tile_offs;       // [E'+1]
+  int32_t* perm_to_src;     // [R']
+  int32_t* src_to_perm;     // [R']
+  int32_t* perm_token;      // [R']
+  int32_t* chunk_counts;    // workspace [nchunks, E]
+  int32_t* chunk_base;      // workspace [nchunks, E]
+};
+int route_tokens_per_chunk(int32_t T);
+int route_num_chunks(int32_t T);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
+                           int32_t k, int32_t shared, int out_dtype, void* out, cudaStream_t s);
+
+enum GemmEpilogue : int { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_SWIGLU_QUANT = 2 };
+
+struct GemmArgs {
+  const uint8_t* a;         // [a_rows, K/2] codes
+  int64_t a_rows;           // capacity of a (rows the TMA may touch)
+  const uint8_t* a_sf;      // grouped-tile layout
+  const uint8_t* b;         // [G, N, K/2]
+  const uint8_t* b_sf;      // MMA layout, N rows per group
+  const float* gs_a;        // [G]
+  const float* gs_b;        // [G]
+  const int32_t* offsets;   // [G+1]
+  const int32_t* tile_offs; // [G+1]
+  int32_t G, N, K;
+  int epilogue;
+  void* d;                  // STORE: [rows, ldd]
+  int64_t ldd;
+  uint8_t* q_codes;         // SWIGLU: [a_rows, N/4]
+  uint8_t* q_sf;            // SWIGLU: grouped-tile layout with K2 = N/2
+  const float* gs_q;        // SWIGLU: [G]
+  float* h_dump;            // SWIGLU: nullable [a_rows, N/2]
+  int* err;                 // device error word
+  int max_ctas;             // 0: one CTA per SM
+};
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** why);
+
+int* device_error_word();   // per current device, nullptr on failure
+int sm_count();
+
+}  // namespace nvf

@@ -1,0 +1,207 @@
+"""End-to-end GPU parity of nvfp4_moe_forward against the oracle.
+
+Bit-exact: routing ids, offsets, permutation, A1 codes and scales, expert
+weight codes and scales, and A2 requantized from the GPU's own h.  Within
+5e-3 * rms(oracle): h, y and out (FP32 output; BF16 output adds one BF16
+rounding).  Against the oracle's own A2 (from the oracle's h, which differs
+from the GPU's h in the last bits) at most a 1e-4 fraction of codes may
+differ, each by one E2M1 step.  Large layers are checked on sampled tokens:
+the oracle evaluates only the experts those tokens visit.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import moe as M
+from synth import CONFIGS, expert_weights, make_inputs
+from tests import oracle_pool
+from tests.nvf_testutil import ROOT, ensure_built, rel_err, unswizzle_grouped, unswizzle_mma, w13_prepared_rows
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+SCALES = json.load(open(os.path.join(ROOT, "tests", "golden", "activation_scales.json")))
+_PREPARED = {}
+
+
+@pytest.fixture(scope="module")
+def nvf():
+    ensure_built()
+    import nvfp4_moe_grouped_router_gb300 as m
+    return m
+
+
+class Layer:
+    """A synthetic layer.  Weights are drawn on `wdev` ("cpu": the CPU generator,
+    uploaded; "cuda": torch's CUDA generator) and prepared by the library; the
+    oracle quantizes its own copy of every expert it needs."""
+
+    def __init__(self, nvf, cfg, seed=0, parent=None, wdev="cpu"):
+        self.nvf, self.cfg, self.seed, self.wdev = nvf, cfg, seed, wdev
+        self.x, self.logits, self.bias = make_inputs(cfg, seed, device="cuda")
+        key = (cfg.H, cfg.I, cfg.E, cfg.shared, seed, wdev)
+        if key not in _PREPARED:
+            _PREPARED.clear()   # keep one weight set resident
+            w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, cfg.shared,
+                                    lambda e: expert_weights(cfg, e, seed, device=wdev))
+            _PREPARED[key] = (w, {})
+        self.wts, self.ocache = _PREPARED[key]
+        sc = SCALES[parent or cfg.name]
+        self.gs_a1 = np.full(cfg.E_total, sc["gs_a1"], np.float32)
+        self.gs_a2 = np.full(cfg.E_total, sc["gs_a2"], np.float32)
+
+    def need(self, experts):
+        todo = [e for e in experts if e not in self.ocache]
+        if not todo:
+            return
+        if self.wdev == "cpu":
+            self.ocache.update(oracle_pool.quantize_generated(self.cfg, todo, self.seed))
+        else:
+            for i in range(0, len(todo), 16):
+                pairs = {e: tuple(t.cpu().numpy() for t in expert_weights(self.cfg, e, self.seed, device="cuda"))
+                         for e in todo[i:i + 16]}
+                self.ocache.update(oracle_pool.quantize_arrays(pairs))
+
+    def run(self, out_dtype=torch.float32, h_dump=True, ws=None):
+        cfg, nvf = self.cfg, self.nvf
+        L = nvf.workspace_layout(cfg.T, cfg.E, cfg.H, cfg.I, cfg.k, cfg.shared)
+        if ws is None:
+            ws = torch.zeros(max(L["total"], 256), dtype=torch.uint8, device="cuda")
+        h = torch.full((L["R"], cfg.I), float("nan"), device="cuda") if h_dump else None
+        out = nvf.moe_forward(self.wts, self.x, self.logits, cfg.k, torch.tensor(self.gs_a1, device="cuda"),
+                              torch.tensor(self.gs_a2, device="cuda"), bias=self.bias,
+                              renormalize=cfg.renormalize, out_dtype=out_dtype, h_dump=h, ws=ws)
+        code, detail = nvf.device_status()
+        assert code == 0, f"device error word {code} at {detail}"
+        return out, ws, L, h
+
+
+def _ws_view(ws, L, name, n, dtype):
+    return ws[L[name]:L[name] + n * np.dtype(dtype).itemsize].cpu().numpy().view(dtype)
+
+
+def check_layer(nvf, layer, out_dtype=torch.float32, tokens=None):
+    cfg = layer.cfg
+    out, ws, L, h_gpu = layer.run(out_dtype)
+    R, Et = L["R"], cfg.E_total
+    xf = layer.x.float().cpu().numpy()
+    lg = layer.logits.cpu().numpy()
+    bias = None if layer.bias is None else layer.bias.cpu().numpy()
+    ids, _ = M.route(lg, bias, cfg.k, cfg.renormalize)
+    if tokens is None:
+        experts = sorted(set(ids.reshape(-1).tolist()) | ({cfg.E} if cfg.shared else set()))
+    else:
+        experts = sorted(set(ids[tokens].reshape(-1).tolist()) | ({cfg.E} if cfg.shared else set()))
+    layer.need(experts)
+    ref = M.moe_forward(xf, lg, bias, cfg.k, cfg.renormalize, cfg.shared, lambda e: layer.ocache[e],
+                        layer.gs_a1, layer.gs_a2, experts=None if tokens is None else set(experts))
+    offs = _ws_view(ws, L, "expert_offsets", Et + 1, np.int32)
+    tiles = _ws_view(ws, L, "tile_offsets", Et + 1, np.int32)
+    assert np.array_equal(_ws_view(ws, L, "topk_ids", cfg.T * cfg.k, np.int32).reshape(cfg.T, cfg.k), ref["ids"])
+    assert np.allclose(_ws_view(ws, L, "topk_w", cfg.T * cfg.k, np.float32).reshape(cfg.T, cfg.k), ref["weights"],
+                       rtol=1e-6, atol=1e-7)
+    assert np.array_equal(offs, ref["offsets"])
+    assert np.array_equal(_ws_view(ws, L, "perm_to_src", R, np.int32), ref["perm_to_src"])
+    assert np.array_equal(_ws_view(ws, L, "src_to_perm", R, np.int32), ref["src_to_perm"])
+    rows = np.zeros(R, bool)
+    for e in experts:
+        rows[offs[e]:offs[e + 1]] = True
+    a1c = ws[L["a1_codes"]:L["a1_codes"] + R * cfg.H // 2].cpu().numpy().reshape(R, cfg.H // 2)
+    a1s = unswizzle_grouped(ws[L["a1_sf"]:].cpu().numpy(), offs, tiles, cfg.H)
+    a2c = ws[L["a2_codes"]:L["a2_codes"] + R * cfg.I // 2].cpu().numpy().reshape(R, cfg.I // 2)
+    a2s = unswizzle_grouped(ws[L["a2_sf"]:].cpu().numpy(), offs, tiles, cfg.I)
+    y = _ws_view(ws, L, "y", R * cfg.H, np.float32).reshape(R, cfg.H)
+    h = h_gpu.cpu().numpy()
+    assert np.array_equal(a1c[rows], ref["a1_codes"][rows])
+    assert np.array_equal(a1s[rows], ref["a1_scales"][rows])
+    # prepared weights equal the oracle's quantization (w13 rows reordered)
+    perm = w13_prepared_rows(cfg.I)
+    n13, n2 = 2 * cfg.I * cfg.H // 16, cfg.H * cfg.I // 16
+    for e in experts[:3] + experts[-2:]:
+        c13, s13, g13, c2, s2, g2 = layer.ocache[e]
+        assert np.array_equal(layer.wts.w13[e].cpu().numpy(), c13[perm])
+        assert np.array_equal(unswizzle_mma(layer.wts.w13_sf[e * n13:(e + 1) * n13].cpu().numpy(), 2 * cfg.I, cfg.H),
+                              s13[perm])
+        assert np.array_equal(layer.wts.w2[e].cpu().numpy(), c2)
+        assert np.array_equal(unswizzle_mma(layer.wts.w2_sf[e * n2:(e + 1) * n2].cpu().numpy(), cfg.H, cfg.I), s2)
+        assert layer.wts.gs_w13[e].item() == g13 and layer.wts.gs_w2[e].item() == g2
+    assert rel_err(h[rows], ref["h"][rows]) <= TOL
+    # A2 from the GPU's own h: bit-exact through the oracle's quantizer
+    gs2_rows = np.repeat(layer.gs_a2, np.diff(offs))
+    qc, qs = F.quantize_rows(h[rows], gs2_rows[rows])
+    assert np.array_equal(a2c[rows], qc)
+    assert np.array_equal(a2s[rows], qs)
+    # against the oracle's own A2: rare one-step flips at rounding boundaries
+    gq = F.unpack_codes(a2c[rows]).astype(int)
+    oq = F.unpack_codes(ref["a2_codes"][rows]).astype(int)
+    diff = gq != oq
+    assert diff.mean() <= 1e-4, diff.mean()
+    if diff.any():
+        steps = np.abs(F.e2m1_decode(gq[diff]) - F.e2m1_decode(oq[diff]))
+        assert np.all(steps <= 2.0)
+    assert rel_err(y[rows], ref["y"][rows]) <= TOL
+    tsel = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+    o = out.float().cpu().numpy()[tsel]
+    r = ref["out"][tsel]
+    rms = np.sqrt(np.mean(ref["out"][tsel] ** 2))
+    if out_dtype == torch.float32:
+        assert np.max(np.abs(o - r)) <= TOL * rms
+    else:
+        assert np.all(np.abs(o - r) <= TOL * rms + np.abs(r) * 2.0 ** -8)
+    return out
+
+
+def _sample_tokens(cfg, logits, bias, n=3):
+    """Tokens whose expert sets overlap most (keeps the oracle's work small)."""
+    ids, _ = M.route(logits.cpu().numpy(), None if bias is None else bias.cpu().numpy(), cfg.k, cfg.renormalize)
+    pop = np.bincount(ids.reshape(-1), minlength=cfg.E)
+    score = pop[ids].sum(1)
+    return sorted(np.argsort(-score, kind="stable")[:n - 1].tolist() + [cfg.T - 1])
+
+
+def test_tiny_layer(nvf):
+    layer = Layer(nvf, CONFIGS["tiny"])
+    check_layer(nvf, layer)
+    check_layer(nvf, layer, torch.bfloat16)
+
+
+def test_decode_layer(nvf):
+    check_layer(nvf, Layer(nvf, CONFIGS["decode"]))
+
+
+def test_prefill_layer_scaled(nvf):
+    check_layer(nvf, Layer(nvf, CONFIGS["prefill"].scaled(T=512, name="prefill_T512"), parent="prefill"))
+
+
+@pytest.mark.parametrize("parent,T", [("skewed", 384), ("large", 48)])
+def test_scaled_layers_sampled(nvf, parent, T):
+    cfg = CONFIGS[parent].scaled(T=T, name=f"{parent}_T{T}")
+    layer = Layer(nvf, cfg, parent=parent, wdev="cuda")
+    check_layer(nvf, layer, tokens=_sample_tokens(cfg, layer.logits, layer.bias))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill", "large", "skewed"])
+def test_full_size_sampled(nvf, name):
+    """The bench's full-size layers: routing and permutation in full, everything
+    else on sampled tokens (all rows of every expert they visit)."""
+    cfg = CONFIGS[name]
+    layer = Layer(nvf, cfg, wdev="cuda")
+    check_layer(nvf, layer, tokens=_sample_tokens(cfg, layer.logits, layer.bias, n=2))
+
+
+def test_deterministic(nvf):
+    layer = Layer(nvf, CONFIGS["tiny"].scaled(T=200, name="tiny_T200"), parent="tiny")
+    a = layer.run()[0].cpu()
+    b = layer.run()[0].cpu()
+    assert torch.equal(a, b)
+
+
+def test_empty_batch(nvf):
+    cfg = CONFIGS["tiny"].scaled(T=0, name="tiny_T0")
+    layer = Layer(nvf, cfg, parent="tiny")
+    out = layer.run(h_dump=False)[0]
+    assert out.shape == (0, cfg.H)

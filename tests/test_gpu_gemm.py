@@ -1,0 +1,130 @@
+"""GPU parity of the grouped block-scaled FP4 GEMM (tcgen05) against the oracle.
+
+Operands are built on the host (random codes, or the oracle's quantization of
+random float32 data) and fed unchanged to both sides.  An exact special case
+(power-of-two scales, small K) must match bit for bit; random cases must stay
+within 5e-3 * rms of the oracle's float64 result.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import moe as M
+from tests.nvf_testutil import ensure_built, grouped_from_rowmajor, mma_from_rowmajor, rel_err
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def nvf():
+    ensure_built()
+    import nvfp4_moe_grouped_router_gb300 as m
+    return m
+
+
+def _pack(q):
+    return (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _run(nvf, a_codes, a_scales, sizes, w_codes, w_scales, gs_a, gs_w, out_dtype=torch.float32, pad_rows=0):
+    sizes = np.asarray(sizes, np.int64)
+    G, N, Kh = w_codes.shape
+    K = 2 * Kh
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    tiles = M.tile_offsets(sizes)
+    R = int(offs[-1])
+    rows = R + pad_rows
+    A = np.zeros((max(rows, 1), Kh), np.uint8)
+    A[:R] = a_codes
+    nbytes = nvf.grouped_scale_bytes(max(rows, 1), G, K)
+    a_sf = grouped_from_rowmajor(a_scales, offs, tiles, K, nbytes)
+    b_sf = mma_from_rowmajor(w_scales.reshape(G * N, K // 16), G * N, K)
+    dev = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    D = nvf.grouped_gemm(dev(A), dev(a_sf), dev(w_codes), dev(b_sf), dev(np.asarray(gs_a, np.float32)),
+                         dev(np.asarray(gs_w, np.float32)), dev(offs.astype(np.int32)), dev(tiles.astype(np.int32)),
+                         N, K, out_dtype)
+    code, detail = nvf.device_status()
+    assert code == 0, f"device error word {code} at {detail}"
+    return D.float().cpu().numpy()[:R], offs
+
+
+def test_exact_special_case(nvf):
+    """E2M1 codes x scales in {1/2, 1, 2}: every partial sum is exact in FP32,
+    so the GPU must equal the oracle bit for bit.  Distinct per-row, per-block
+    scales and asymmetric codes pin the nibble order and the scale-atom layout."""
+    rng = np.random.default_rng(0)
+    sizes = [130, 0, 1, 127, 128]
+    G, N, K = len(sizes), 256, 512
+    R = sum(sizes)
+    q_a = rng.integers(0, 16, (R, K)).astype(np.uint8)
+    q_w = rng.integers(0, 16, (G, N, K)).astype(np.uint8)
+    s_choices = np.array([0x30, 0x38, 0x40], np.uint8)   # 0.5, 1, 2
+    s_a = s_choices[rng.integers(0, 3, (R, K // 16))]
+    s_w = s_choices[rng.integers(0, 3, (G, N, K // 16))]
+    D, offs = _run(nvf, _pack(q_a), s_a, sizes, _pack(q_w), s_w, np.ones(G), np.ones(G))
+    ref = M.grouped_gemm(_pack(q_a), s_a, offs, np.ones(G, np.float32), _pack(q_w), s_w, np.ones(G, np.float32))
+    assert np.array_equal(D, ref.astype(np.float32)), f"max abs diff {np.max(np.abs(D - ref))}"
+
+
+def test_exact_single_element_probes(nvf):
+    """One nonzero code per row at a chosen K position and one nonzero scale
+    block: locates each K index and each scale byte exactly."""
+    G, N, K = 1, 128, 256
+    R = 128
+    q_a = np.zeros((R, K), np.uint8)
+    s_a = np.full((R, K // 16), 0x38, np.uint8)
+    for r in range(R):
+        q_a[r, (r * 37) % K] = 2          # value 1.0 at one K position per row
+        s_a[r, (r * 37 % K) // 16] = 0x40  # its block scale 2.0
+    q_w = np.zeros((G, N, K), np.uint8)
+    s_w = np.full((G, N, K // 16), 0x38, np.uint8)
+    for n in range(N):
+        q_w[0, n, :] = (n % 7) + 1         # distinct positive values per column
+        s_w[0, n, n % (K // 16)] = 0x30
+    D, offs = _run(nvf, _pack(q_a), s_a, [R], _pack(q_w), s_w, [1.0], [1.0])
+    ref = M.grouped_gemm(_pack(q_a), s_a, offs, np.ones(1, np.float32), _pack(q_w), s_w, np.ones(1, np.float32))
+    assert np.array_equal(D, ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("sizes,N,K", [
+    ([5], 128, 64),
+    ([0, 1, 127, 128, 129], 256, 256),
+    ([300, 7, 0, 0, 45], 384, 320),
+    ([33, 200], 128, 128),
+    ([1] * 40, 256, 2048),
+    ([8065, 0, 513], 1536, 2048),
+])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_random_within_tolerance(nvf, sizes, N, K, out_dtype):
+    rng = np.random.default_rng(sum(sizes) + N + K)
+    G = len(sizes)
+    R = sum(sizes)
+    a = rng.standard_normal((R, K)).astype(np.float32)
+    gs_a = np.full(G, F.global_scale(np.abs(a).max() if R else 1.0), np.float32)
+    a_c, a_s = F.quantize_rows(a, gs_a[0])
+    w = (rng.standard_normal((G, N, K)) * 0.02).astype(np.float32)
+    qw = [M.quantize_expert_weights(w[g]) for g in range(G)]
+    w_c = np.stack([q[0] for q in qw])
+    w_s = np.stack([q[1] for q in qw])
+    gs_w = np.array([q[2] for q in qw], np.float32)
+    D, offs = _run(nvf, a_c, a_s, sizes, w_c, w_s, gs_a, gs_w, out_dtype, pad_rows=3)
+    ref = M.grouped_gemm(a_c, a_s, offs, gs_a, w_c, w_s, gs_w)
+    err = rel_err(D, ref)
+    if out_dtype == torch.float32:
+        assert err <= TOL, err
+    else:
+        # bf16 output: the same bound plus one bf16 rounding of each element
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.all(np.abs(D - ref) <= TOL * rms + np.abs(ref) * 2.0 ** -8)
+
+
+def test_argument_validation(nvf):
+    z = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    f = torch.ones(1, dtype=torch.float32, device="cuda")
+    o = torch.tensor([0, 0], dtype=torch.int32, device="cuda")
+    with pytest.raises(nvf.NvfError, match="N=100"):
+        nvf.grouped_gemm(z.view(2, 128), z, z.view(1, 2, 128), z, f, f, o, o, 100, 256)
+    with pytest.raises(nvf.NvfError, match="K=100"):
+        nvf.grouped_gemm(z.view(4, 64), z, z.view(1, 2, 128), z, f, f, o, o, 128, 100)
