@@ -91,10 +91,10 @@ def e2m1_encode(y) -> np.ndarray:
 
 def e4m3_encode(v) -> np.ndarray:
     """float32 v >= 0 -> unsigned E4M3 byte: nearest finite value, ties to even,
-    saturating at 448 (what a satfinite conversion does)."""
+    saturating at 448 (what a satfinite conversion does; +inf also gives 448)."""
     v = np.asarray(v, dtype=F32)
-    if np.any(v < 0) or np.any(~np.isfinite(v)):
-        raise ValueError("e4m3_encode expects finite non-negative inputs")
+    if np.any(v < 0) or np.any(np.isnan(v)):
+        raise ValueError("e4m3_encode expects non-negative, non-NaN inputs")
     return _nearest_even(v, _E4M3_POS_VALUES).astype(np.uint8)
 
 
@@ -125,7 +125,8 @@ def quantize_rows(x, gs):
     blocks = x.reshape(rows, K // BLOCK, BLOCK)
     amax = np.max(np.abs(blocks), axis=2)                            # [rows, K/16], exact
     t1 = (F32(6.0) * gs).astype(F32)                                 # [rows, 1]
-    t2 = (amax / t1).astype(F32)
+    with np.errstate(over="ignore"):
+        t2 = (amax / t1).astype(F32)                                 # may overflow to +inf
     sb = e4m3_encode(t2)
     t3 = (e4m3_decode(sb).astype(F32) * gs).astype(F32)
     with np.errstate(divide="ignore"):

@@ -139,7 +139,7 @@ def test_e4m3_exhaustive_bit_patterns_vs_torch():
 
 
 def test_e4m3_saturates():
-    x = np.array([448.0, 449.0, 463.9, 464.0, 480.0, 1e6, 3e38], np.float32)
+    x = np.array([448.0, 449.0, 463.9, 464.0, 480.0, 1e6, 3e38, np.inf], np.float32)
     assert np.all(F.e4m3_encode(x) == 0x7E)
 
 
