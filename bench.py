@@ -1,0 +1,370 @@
+"""Benchmark of the NVFP4 MoE layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl ours|reference]
+
+A step is one pass of the whole layer (route, permute, quantize, gate_up GEMM
+with fused SiLU*up requant, down GEMM, combine) over one batch.  Default
+workload: the 30B-A3B-shaped decode layer (T=32, H=2048, I=768, E=128, top-8).
+Inputs are synthetic (seeded), weights are drawn on the device and prepared by
+the library before timing.  The timed region replays a CUDA graph of the K
+steps; the weights streamed per step (about 300 MB) exceed the 129 MB L2.
+
+Multi-GPU: every rank runs its own replica on its own batch (the layer shards
+by tokens with no exchange): value = tokens of all ranks / max-over-ranks time.
+
+--impl reference times the CPU oracle (the reference arm for this build) on a
+bounded token sample of the same workload, on the host cores.
+"""
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle baseline runs on one core
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import CONFIGS, expert_weights, make_inputs  # noqa: E402
+
+METRIC = "NVFP4 MoE layer tokens/s; grouped-GEMM % FP4 TC peak (prefill) / % HBM (decode)"
+STAGES = ["route_permute", "quantize_a1", "gate_up_gemm_swiglu_quant", "down_gemm", "combine"]
+KERNELS_PER_STEP = 7   # route: topk, scan, scatter; quantize; two GEMMs; combine
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def activation_scales(name):
+    d = json.load(open(os.path.join(ROOT, "tests", "golden", "activation_scales.json")))
+    return d[name]["gs_a1"], d[name]["gs_a2"]
+
+
+def layer_bytes(cfg, counts):
+    """Algorithmic bytes of one step: weights of touched experts (codes + scales +
+    global scales), x, logits and out.  counts: rows per expert (shared included)."""
+    touched = int((np.asarray(counts) > 0).sum())
+    per_expert = 3 * cfg.H * cfg.I * (0.5 + 1.0 / 16) + 8
+    return touched, touched * per_expert + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.H * 4
+
+
+def gemm1_bytes(cfg, touched, R):
+    """Algorithmic bytes of the gate_up GEMM launch: w13 of touched experts, A1 in, A2 out."""
+    return touched * 2 * cfg.I * cfg.H * (0.5 + 1.0 / 16) + R * cfg.H * (0.5 + 1.0 / 16) + R * cfg.I * (0.5 + 1.0 / 16) / 2
+
+
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def start(self):
+        q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        dev = os.environ.get("LOCAL_RANK", "0")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", dev, f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = [r.split(", ") for r in open(self.path).read().strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                s, m, pw = float(r[1]), float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            mx = m
+            if pw > 200:           # under load
+                sm.append(s)
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples_under_load": len(sm)}
+
+
+def oracle_sample(cfg, x, logits, bias, tokens, oracle_w):
+    from oracle import moe as M
+    xs = x[tokens].float().cpu().numpy()
+    ls = logits[tokens].cpu().numpy()
+    b = None if bias is None else bias.cpu().numpy()
+    E = cfg.E_total
+    gs1, gs2 = activation_scales(cfg.name)
+    return M.moe_forward(xs, ls, b, cfg.k, cfg.renormalize, cfg.shared, lambda e: oracle_w[e],
+                         np.full(E, gs1, np.float32), np.full(E, gs2, np.float32))
+
+
+def prepare_oracle_weights(cfg, x, logits, bias, tokens, seed):
+    from oracle import moe as M
+    ids, _ = M.route(logits[tokens].cpu().numpy(), None if bias is None else bias.cpu().numpy(), cfg.k,
+                     cfg.renormalize)
+    experts = sorted(set(ids.reshape(-1).tolist()) | ({cfg.E} if cfg.shared else set()))
+    out = {}
+    for e in experts:
+        w13, w2 = expert_weights(cfg, e, seed, device="cuda" if torch.cuda.is_available() else "cpu")
+        out[e] = (*M.quantize_expert_weights(w13.cpu().numpy()), *M.quantize_expert_weights(w2.cpu().numpy()))
+    return out
+
+
+def cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s):
+    """Tokens/s of the oracle (steps S1-S7, weights prepared beforehand) on a token sample."""
+    tokens = [0]
+    ow = prepare_oracle_weights(cfg, x, logits, bias, tokens, seed)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_sample(cfg, x, logits, bias, tokens, ow)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= 1000:
+            break
+    return n * len(tokens) / dt, f"{n} oracle pass(es) over token 0 of the {cfg.name} batch ({len(ow)} experts)"
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    seed = 0
+    x, logits, bias = make_inputs(cfg, seed, device="cpu")
+    total_budget = 150.0
+    per_step = max(1.0, total_budget / max(1, args.steps + args.warmup))
+    tokens = [0]
+    ow = prepare_oracle_weights(cfg, x, logits, bias, tokens, seed)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, x, logits, bias, tokens, ow)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            oracle_sample(cfg, x, logits, bias, tokens, ow)
+            n += 1
+            if time.perf_counter() - t0 >= per_step * 0.5 or n >= 50:
+                break
+        times.append((time.perf_counter() - t0) / n)
+    ms = 1000 * statistics.mean(times)
+    value = len(tokens) / (ms / 1000)
+    cores = 1
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
+                       "sample_tokens": len(tokens)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"token 0 of the {cfg.name} batch through the CPU oracle (S1-S7), one core"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode", choices=list(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import nvfp4_moe_grouped_router_gb300 as nvf
+    from nvfp4_moe_grouped_router_gb300 import build as nvf_build
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0 or local == 0:
+        nvf_build.build()
+    if dist:
+        dist.barrier()
+    nvf.lib()
+
+    seed = 0
+    x, logits, bias = make_inputs(cfg, seed + rank, device="cuda")
+    w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, cfg.shared, lambda e: expert_weights(cfg, e, seed, device="cuda"))
+    gs1, gs2 = activation_scales(cfg.name)
+    gs_a1 = torch.full((cfg.E_total,), gs1, device="cuda")
+    gs_a2 = torch.full((cfg.E_total,), gs2, device="cuda")
+    ws = nvf.workspace(cfg.T, w, cfg.k)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device="cuda")
+    cw = w.c_struct()
+
+    def step(events=None):
+        nvf.moe_forward(w, x, logits, cfg.k, gs_a1, gs_a2, bias=bias, renormalize=cfg.renormalize, out=out,
+                        ws=ws, stage_events=events, cw=cw)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    code, detail = nvf.device_status()
+    if code != 0:
+        raise RuntimeError(f"device error word {code} at {detail}")
+
+    # --- graph of the K timed steps, with per-stage events inside
+    K = args.steps
+    chunk = min(K, 256)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(chunk)]
+    for row in ev:          # torch creates the CUDA event on first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(stream):
+        for n in sorted({chunk, K % chunk} - {0}, reverse=True):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(ev[i])
+            graphs.append((n, g))
+    torch.cuda.current_stream().wait_stream(stream)
+    plan = [graphs[0]] * (K // chunk) + ([g for g in graphs if g[0] == K % chunk] if K % chunk else [])
+    for n, g in graphs:    # warm the graphs
+        g.replay()
+    torch.cuda.synchronize()
+
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    clocks = ClockSampler(os.path.join(out_dir, f"clocks_rank{rank}.csv") if os.path.isdir(out_dir)
+                          else f"/tmp/nvf_clocks_{os.getpid()}.csv")
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for n, g in plan:
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    t = torch.tensor([elapsed_ms], device="cuda")
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    code, detail = nvf.device_status()
+    if code != 0:
+        raise RuntimeError(f"device error word {code} at {detail}")
+
+    # per-stage durations of the last replayed chunk
+    last_n = plan[-1][0]
+    stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(last_n))
+                for j, s in enumerate(STAGES)}
+
+    # --- end to end through the C ABI with host buffers
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    oh = torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory()
+    xd, ld = torch.empty_like(x), torch.empty_like(logits)
+    Ke = min(K, 200)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        nvf.moe_forward(w, xd, ld, cfg.k, gs_a1, gs_a2, bias=bias, renormalize=cfg.renormalize, out=out, ws=ws,
+                        cw=cw)
+        oh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    # --- roofline of the dominant kernel
+    L = nvf.workspace_layout(cfg.T, cfg.E, cfg.H, cfg.I, cfg.k, cfg.shared)
+    offs = ws[L["expert_offsets"]:L["expert_offsets"] + 4 * (cfg.E_total + 1)].view(torch.int32).cpu().numpy()
+    touched, lbytes = layer_bytes(cfg, np.diff(offs))
+    dominant = max(stage_ms, key=stage_ms.get)
+    hbm, bf16, src = load_peaks()
+    R = cfg.R
+    g1 = gemm1_bytes(cfg, touched, R)
+    flops_g1 = 4.0 * R * cfg.H * cfg.I
+    fp4_peak_tflops = bf16 * 6.0           # dense FP4 / BF16 nominal ratio (13.5 / 2.25)
+    if dominant == "gate_up_gemm_swiglu_quant":
+        ach = g1 / (stage_ms[dominant] * 1e-3) / 1e9
+        roof = {"kernel": "grouped_gemm_kernel<SWIGLU_QUANT> (gate_up)", "bound": "hbm", "achieved": ach,
+                "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic_from_profiles(cfg.name),
+                "algorithmic_bytes": g1, "peak_source": src,
+                "tflops": flops_g1 / (stage_ms[dominant] * 1e-3) / 1e12,
+                "tc_frac_fp4": flops_g1 / (stage_ms[dominant] * 1e-3) / 1e12 / fp4_peak_tflops}
+    else:
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
+                "traffic": None}
+
+    ms_step = elapsed_ms / K
+    value = cfg.T * world / (ms_step * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales) -> f32", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: {cfg.description} (T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E}"
+                                   f"{'+1 shared' if cfg.shared else ''} top-{cfg.k})",
+                       "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "shared": cfg.shared,
+                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (weights streamed per step)",
+                       "timing": "CUDA graph of the K steps, CUDA events"},
+            "stage_ms": stage_ms, "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
+            "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
+            "roofline": roof, "clocks": clk, "gpu_launches": KERNELS_PER_STEP * K,
+            "e2e": {"value": cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                    "d2h_bytes_per_step": out.numel() * 4}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample = cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s=10.0)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def traffic_from_profiles(name):
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    from nvfp4_moe_grouped_router_gb300 import build as b
+    import hashlib
+    h = hashlib.sha256(open(os.path.join(b.CSRC, "gemm.cu"), "rb").read()).hexdigest()[:16]
+    e = d.get(name)
+    if not e or e.get("gemm_cu_sha") != h:
+        return None
+    return e.get("bytes_per_launch")
+
+
+if __name__ == "__main__":
+    main()

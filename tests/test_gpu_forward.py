@@ -155,11 +155,12 @@ def check_layer(nvf, layer, out_dtype=torch.float32, tokens=None):
 
 
 def _sample_tokens(cfg, logits, bias, n=3):
-    """Tokens whose expert sets overlap most (keeps the oracle's work small)."""
+    """The n-1 tokens whose experts hold the fewest rows, plus the last token
+    (keeps the oracle's work small: it evaluates every row of those experts)."""
     ids, _ = M.route(logits.cpu().numpy(), None if bias is None else bias.cpu().numpy(), cfg.k, cfg.renormalize)
     pop = np.bincount(ids.reshape(-1), minlength=cfg.E)
     score = pop[ids].sum(1)
-    return sorted(np.argsort(-score, kind="stable")[:n - 1].tolist() + [cfg.T - 1])
+    return sorted(set(np.argsort(score, kind="stable")[:n - 1].tolist() + [cfg.T - 1]))
 
 
 def test_tiny_layer(nvf):
