@@ -190,6 +190,8 @@ def main():
     ap.add_argument("--config", default="decode", choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="plain launches of W + K steps and nothing else (for ncu launch lists / captures)")
     args = ap.parse_args()
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
@@ -231,6 +233,15 @@ def main():
     code, detail = nvf.device_status()
     if code != 0:
         raise RuntimeError(f"device error word {code} at {detail}")
+    if args.profile:
+        for _ in range(args.steps):
+            step()
+        code, detail = nvf.device_status()
+        if code != 0:
+            raise RuntimeError(f"device error word {code} at {detail}")
+        print(json.dumps({"profile_run": cfg.name, "steps": args.steps, "warmup": max(3, args.warmup),
+                          "kernels_per_step": KERNELS_PER_STEP}))
+        return
 
     # --- graph of the K timed steps, with per-stage events inside
     K = args.steps
@@ -260,7 +271,13 @@ def main():
     clocks = ClockSampler(os.path.join(out_dir, f"clocks_rank{rank}.csv") if os.path.isdir(out_dir)
                           else f"/tmp/nvf_clocks_{os.getpid()}.csv")
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
+    # Soak (untimed): replay the same graph for ~1 s so that the clock samples
+    # taken around the (often millisecond-long) timed region see the load.
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        plan[0][1].replay()
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()

@@ -337,7 +337,9 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   auto i32 = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
   const int nch = route_num_chunks(T);
   auto mark = [&](int i) -> cudaError_t {
-    return stage_events ? cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s) : cudaSuccess;
+    // External records become event nodes when the stream is being captured into a graph.
+    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal)
+                        : cudaSuccess;
   };
   NVF_CUDA(mark(0), "cudaEventRecord");
 

@@ -89,3 +89,67 @@ def rel_err(got, ref) -> float:
     ref = np.asarray(ref, np.float64)
     rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
     return float(np.max(np.abs(got - ref)) / rms) if ref.size and rms > 0 else float(np.max(np.abs(got - ref), initial=0))
+
+
+# ----------------------------------------------------------------------------- independent quantizer
+# A second statement of NVFP4 block quantization, written from the threshold
+# table (E2M1) and the quantum-and-round formula (E4M3) rather than the
+# oracle's nearest-value search.  The tests use it to check that a GPU
+# intermediate (the requantized h) is a valid quantization of the GPU's own
+# values without feeding GPU data into the oracle.
+def e2m1_threshold_encode(y):
+    y = np.asarray(y, dtype=np.float32)
+    v = np.abs(y)
+    m = np.select([v <= 0.25, v < 0.75, v <= 1.25, v < 1.75, v <= 2.5, v < 3.5, v <= 5.0], [0, 1, 2, 3, 4, 5, 6], 7)
+    return (m | (np.signbit(y).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def e4m3_formula_encode(v):
+    v = np.asarray(v, dtype=np.float64)
+    out = np.zeros(v.shape, np.int64)
+    sat = v >= 448.0
+    sub = v < 2.0 ** -6
+    out[sub] = np.rint(v[sub] * 512.0).astype(np.int64)
+    nrm = ~sat & ~sub
+    mant, ex = np.frexp(v[nrm])                 # v = mant * 2^ex, mant in [0.5, 1)
+    e = ex - 1                                  # floor(log2 v)
+    n = np.rint(v[nrm] / np.ldexp(1.0, e - 3)).astype(np.int64)
+    carry = n == 16
+    e = np.where(carry, e + 1, e)
+    n = np.where(carry, 8, n)
+    out[nrm] = np.minimum(((e + 7) << 3) | (n - 8), 0x7E)
+    out[sat] = 0x7E
+    return out.astype(np.uint8)
+
+
+def e4m3_formula_decode(b):
+    b = np.asarray(b, dtype=np.int64)
+    e, m = (b >> 3) & 0xF, b & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.ldexp(1.0, e - 7))
+
+
+def quantize_rows_check(x, gs):
+    f32 = np.float32
+    x = np.asarray(x, dtype=f32)
+    rows, K = x.shape
+    gs = np.broadcast_to(np.asarray(gs, dtype=f32).reshape(-1, 1), (rows, 1)).astype(f32)
+    b = x.reshape(rows, K // 16, 16)
+    amax = np.abs(b).max(axis=2)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        t2 = (amax / (f32(6.0) * gs).astype(f32)).astype(f32)
+        sb = e4m3_formula_encode(t2)
+        t3 = (e4m3_formula_decode(sb).astype(f32) * gs).astype(f32)
+        r = np.where(t3 == 0, f32(0), f32(1.0) / t3).astype(f32)
+        q = e2m1_threshold_encode((b * r[:, :, None]).astype(f32)).reshape(rows, K)
+    return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8), sb
+
+
+def dequant_check(codes, scales):
+    """Dequantized NVFP4 rows without the global scale, from the formulas above."""
+    c = np.asarray(codes, dtype=np.uint8)
+    q = np.empty(c.shape[:-1] + (c.shape[-1] * 2,), np.int64)
+    q[..., 0::2] = c & 0xF
+    q[..., 1::2] = c >> 4
+    mag = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])[q & 7]
+    val = np.where(q & 8, -mag, mag)
+    return val * np.repeat(e4m3_formula_decode(scales), 16, axis=-1)

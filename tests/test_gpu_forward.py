@@ -1,12 +1,16 @@
 """End-to-end GPU parity of nvfp4_moe_forward against the oracle.
 
-Bit-exact: routing ids, offsets, permutation, A1 codes and scales, expert
-weight codes and scales, and A2 requantized from the GPU's own h.  Within
-5e-3 * rms(oracle): h, y and out (FP32 output; BF16 output adds one BF16
-rounding).  Against the oracle's own A2 (from the oracle's h, which differs
-from the GPU's h in the last bits) at most a 1e-4 fraction of codes may
-differ, each by one E2M1 step.  Large layers are checked on sampled tokens:
-the oracle evaluates only the experts those tokens visit.
+Bit-exact against the oracle: routing ids, offsets, permutation, A1 codes
+and scales, expert weight codes, scales and global scales.  Within
+5e-3 * rms(oracle): routing weights (1e-6 relative), h, y and out (FP32
+output; BF16 output adds one BF16 rounding).
+A2 (the requantized h) is not unique: GPU and oracle sum GEMM1 in different
+orders, so an h on a rounding boundary may round either way.  The test checks
+that the GPU's A2 is exactly the quantization of the GPU's own h (with an
+independent checker, not the oracle), that codes differing from the oracle's
+A2 are rare (<= 1e-4), and that y / out differ from the oracle by at most the
+tolerance plus what those flips explain.  Large layers are checked on sampled
+tokens: the oracle evaluates only the experts those tokens visit.
 """
 import json
 import os
@@ -19,7 +23,8 @@ from oracle import formats as F
 from oracle import moe as M
 from synth import CONFIGS, expert_weights, make_inputs
 from tests import oracle_pool
-from tests.nvf_testutil import ROOT, ensure_built, rel_err, unswizzle_grouped, unswizzle_mma, w13_prepared_rows
+from tests.nvf_testutil import (ROOT, dequant_check, ensure_built, quantize_rows_check, rel_err, unswizzle_grouped,
+                                 unswizzle_mma, w13_prepared_rows)
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -129,28 +134,50 @@ def check_layer(nvf, layer, out_dtype=torch.float32, tokens=None):
         assert np.array_equal(unswizzle_mma(layer.wts.w2_sf[e * n2:(e + 1) * n2].cpu().numpy(), cfg.H, cfg.I), s2)
         assert layer.wts.gs_w13[e].item() == g13 and layer.wts.gs_w2[e].item() == g2
     assert rel_err(h[rows], ref["h"][rows]) <= TOL
-    # A2 from the GPU's own h: bit-exact through the oracle's quantizer
+    # A2 is a valid requantization of the GPU's own h (independent checker, bit-exact)
     gs2_rows = np.repeat(layer.gs_a2, np.diff(offs))
-    qc, qs = F.quantize_rows(h[rows], gs2_rows[rows])
+    qc, qs = quantize_rows_check(h[rows], gs2_rows[rows])
     assert np.array_equal(a2c[rows], qc)
     assert np.array_equal(a2s[rows], qs)
-    # against the oracle's own A2: rare one-step flips at rounding boundaries
-    gq = F.unpack_codes(a2c[rows]).astype(int)
-    oq = F.unpack_codes(ref["a2_codes"][rows]).astype(int)
-    diff = gq != oq
-    assert diff.mean() <= 1e-4, diff.mean()
-    if diff.any():
-        steps = np.abs(F.e2m1_decode(gq[diff]) - F.e2m1_decode(oq[diff]))
-        assert np.all(steps <= 2.0)
-    assert rel_err(y[rows], ref["y"][rows]) <= TOL
+    # Against the oracle's own A2 (from its float64 h): GPU and oracle sum GEMM1
+    # in different orders, so an h that sits on a rounding boundary may round
+    # either way; both results are correct.  Such flips must be rare.
+    code_diff = F.unpack_codes(a2c[rows]) != F.unpack_codes(ref["a2_codes"][rows])
+    assert code_diff.mean() <= 1e-4, code_diff.mean()
+    row_diff = np.zeros(R, bool)
+    row_diff[rows] = code_diff.any(1) | (a2s[rows] != ref["a2_scales"][rows]).any(1)
+    assert row_diff.sum() <= max(2, 0.02 * rows.sum()), row_diff.sum()
+    # y: rows with identical A2 within 5e-3 * rms; a row whose A2 flipped may
+    # differ further by exactly what the flip explains, alpha2 * |W2| . |dA2 - dA2_oracle|.
+    y_rms = np.sqrt(np.mean(ref["y"][rows] ** 2))
+    explained = np.zeros((R, cfg.H))
+    for p in np.nonzero(row_diff)[0]:
+        e = int(np.searchsorted(offs, p, side="right") - 1)
+        c13, s13, g13, c2, s2, g2 = layer.ocache[e]
+        d = np.abs(dequant_check(a2c[p:p + 1], a2s[p:p + 1]) - dequant_check(ref["a2_codes"][p:p + 1],
+                                                                             ref["a2_scales"][p:p + 1]))[0]
+        alpha2 = float(np.float32(np.float32(layer.gs_a2[e]) * np.float32(g2)))
+        explained[p] = alpha2 * (np.abs(dequant_check(c2, s2)) @ d)
+    same = rows & ~row_diff
+    assert np.max(np.abs(y[same] - ref["y"][same]), initial=0) <= TOL * y_rms
+    assert np.all(np.abs(y[rows] - ref["y"][rows]) <= TOL * y_rms + 1.001 * explained[rows])
+    # out: the same bound, each row's explained part weighted by its routing weight
     tsel = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
+    s2p = ref["src_to_perm"]
+    w = ref["weights"]
+    ex_out = np.zeros((cfg.T, cfg.H))
+    for t in tsel:
+        for j in range(cfg.k):
+            ex_out[t] += w[t, j] * explained[s2p[t * cfg.k + j]]
+        if cfg.shared:
+            ex_out[t] += explained[s2p[cfg.T * cfg.k + t]]
     o = out.float().cpu().numpy()[tsel]
     r = ref["out"][tsel]
-    rms = np.sqrt(np.mean(ref["out"][tsel] ** 2))
-    if out_dtype == torch.float32:
-        assert np.max(np.abs(o - r)) <= TOL * rms
-    else:
-        assert np.all(np.abs(o - r) <= TOL * rms + np.abs(r) * 2.0 ** -8)
+    rms = np.sqrt(np.mean(r ** 2))
+    slack = TOL * rms + 1.001 * ex_out[tsel]
+    if out_dtype == torch.bfloat16:
+        slack = slack + np.abs(r) * 2.0 ** -8     # one bf16 rounding of the output
+    assert np.all(np.abs(o - r) <= slack)
     return out
 
 
