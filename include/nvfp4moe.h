@@ -142,6 +142,35 @@ nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, 
                              int32_t* expert_offsets, int32_t* tile_offsets, int32_t* perm_to_src,
                              int32_t* src_to_perm, int32_t* perm_token, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route_permute for callers that cannot allocate device memory.  (The
+ * source pages have no counterpart: this is a library convenience.)
+ * Some callers have no way to hand this library scratch memory: code that runs
+ * inside a framework whose caching allocator owns every device allocation,
+ * plug-ins that are given only their input and output buffers, or
+ * latency-critical loops where a cudaMalloc (and the device-wide
+ * synchronisation it can imply) is not acceptable.  This entry point takes the
+ * same inputs and outputs as moe_route_permute but no workspace: its scratch
+ * is a fixed 2 MiB array in device memory that the library reserves on every
+ * GPU that loads it, for the life of the process.
+ *   - Sizes: the scratch needed (moe_route_permute_workspace_size(T, E)) must
+ *     not exceed NVF_ROUTE_STATIC_SCRATCH_BYTES; larger calls return
+ *     NVF_ERR_WORKSPACE before any launch (about T*E <= 2^24, e.g. 65536 tokens
+ *     with 256 experts).
+ *   - Allocation: none.  No cudaMalloc/cudaFree or allocating library call is
+ *     made.  The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     outside any stream capture.
+ *   - Sharing: every call on a device uses the same array, and the array keeps
+ *     the last call's contents.  Nothing in it has to start at zero (each call
+ *     overwrites every byte it reads).  Calls that can overlap on the GPU (on
+ *     different streams without ordering between them) race on the array and
+ *     must be serialised by the caller. */
+#define NVF_ROUTE_STATIC_SCRATCH_BYTES (2u << 20)
+nvf_status moe_route_permute_noalloc(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k,
+                                     int32_t renormalize, int32_t shared_expert, int32_t* topk_ids, float* topk_w,
+                                     int32_t* expert_offsets, int32_t* tile_offsets, int32_t* perm_to_src,
+                                     int32_t* src_to_perm, int32_t* perm_token, void* stream);
+
 /* Grouped block-scaled FP4 GEMM (steps 4 / 6 with a plain epilogue):
  *   D[row, n] = gs_a[g] * gs_b[g] * sum_k A[row, k] B[g, n, k]   for offsets[g] <= row < offsets[g+1].
  *   A       device uint8[a_rows, K/2] codes; a_rows bounds every row the GEMM may

@@ -38,6 +38,8 @@ SIGNATURES = {
     "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
                                           _P]),
     "nvfp4_moe_workspace_layout": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
+    "moe_route_permute_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                                 _P]),
     "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
                                          _P]),
 }

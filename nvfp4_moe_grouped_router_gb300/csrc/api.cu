@@ -77,6 +77,9 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
 int sm_count() { return g_cur_sms; }
+void set_last_error(const char* msg) {
+  std::snprintf(g_msg, sizeof(g_msg), "%s", msg);
+}
 int* device_error_word() {
   DeviceInfo* di = nullptr;
   return current_device(&di) == NVF_OK ? di->err : nullptr;
