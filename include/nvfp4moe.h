@@ -26,20 +26,29 @@
  *     64-element MMA step (one scale per 16 elements).
  *
  * NVFP4 data (everywhere in this ABI):
- *   codes  : uint8, two E2M1 codes per byte, K-index 2j in bits 0-3 of byte j.
- *   scales : uint8 E4M3 (unsigned) per 16 consecutive K elements.
+ *   codes  : two E2M1 codes per byte, K-index 2j in bits 0-3 of byte j.
+ *   scales : one unsigned E4M3 byte per 16 consecutive K elements.
  *   gs     : float32 per-tensor (or per-expert) decode scale; value = e2m1 *
  *            e4m3 * gs.  A block scale is E4M3(amax_block / (6 * gs)).
- * Scale layouts (enum nvf_sf_layout):
- *   NVF_SF_ROWMAJOR : [rows][K/16].
- *   NVF_SF_MMA      : 512-byte atoms of 128 rows x 4 scales; atom (row/128,
- *                     k64 = K-index/64) at byte ((row/128)*(K/64) + k64)*512,
- *                     row r (mod 128), scale b (0..3) inside it at
- *                     (r%32)*16 + (r/32)*4 + b.  Buffer: ceil(rows/128)*128*K/16 B.
- *   NVF_SF_GROUPED  : rows grouped by offsets[G+1]; group g's rows form 128-row
- *                     tiles numbered from tile_offsets[g] (exclusive prefix of
- *                     ceil(m_g/128)); atom (tile, k64) at (tile*(K/64) + k64)*512.
- *                     Buffer: nvfp4_grouped_scale_bytes(rows, G, K).
+ * Operand layouts (enum nvf_layout):
+ *   NVF_LAYOUT_ROWMAJOR      : codes uint8[rows][K/2], scales uint8[rows][K/16].
+ *   NVF_LAYOUT_TILED         : one buffer of 18432-byte chunks, chunk (tile, kt)
+ *                              at (tile * nkt + kt) * 18432, tile = row / 128,
+ *                              nkt = ceil(K / 256).  A chunk holds K elements
+ *                              [256 kt, 256 kt + 256) of 128 rows:
+ *                              bytes [0, 16384): codes, 128 per row, code byte b
+ *                                of row r at r*128 + (((b/16) ^ (r%8))*16) + b%16;
+ *                              bytes [16384, 18432): four 512-byte scale atoms,
+ *                                atom kk for K elements [64 kk, 64 kk + 64) of the
+ *                                chunk, scale s (0..3) of row r at
+ *                                (r%32)*16 + (r/32)*4 + s.
+ *                              Size: nvfp4_tiled_bytes(rows, 0, K).
+ *   NVF_LAYOUT_TILED_GROUPED : as TILED, but rows grouped by offsets[G+1]:
+ *                              group g's rows form 128-row tiles numbered from
+ *                              tile_offsets[g] (exclusive prefix of
+ *                              ceil(m_g / 128)).  Size: nvfp4_tiled_bytes(rows, G, K).
+ *   Bytes of rows past a group's end, and of K past K in the last chunk, are
+ *   neither written nor read as data.
  *
  * Conventions.  All pointers marked "device" are device memory owned by the
  * caller; the library never allocates, frees or synchronises on these paths.
@@ -72,7 +81,11 @@ typedef enum nvf_status {
 } nvf_status;
 
 typedef enum nvf_dtype { NVF_F32 = 0, NVF_BF16 = 1 } nvf_dtype;
-typedef enum nvf_sf_layout { NVF_SF_ROWMAJOR = 0, NVF_SF_MMA = 1, NVF_SF_GROUPED = 2 } nvf_sf_layout;
+typedef enum nvf_layout {
+  NVF_LAYOUT_ROWMAJOR = 0,
+  NVF_LAYOUT_TILED = 1,
+  NVF_LAYOUT_TILED_GROUPED = 2
+} nvf_layout;
 
 /* Name of a status code (static string). */
 const char* nvf_status_string(nvf_status s);
@@ -97,8 +110,9 @@ nvf_status nvf_device_status(void* stream, int32_t* code, int32_t* detail);
  * [16c, 16c+16).  map: host int32[2I].  I must be a positive multiple of 64. */
 nvf_status nvf_w13_row_map(int32_t I, int32_t* map);
 
-/* Bytes of an NVF_SF_GROUPED scale buffer for up to `rows` rows in G groups. */
-size_t nvfp4_grouped_scale_bytes(int64_t rows, int32_t G, int32_t K);
+/* Bytes of a tiled operand buffer for up to `rows` rows, K columns and G
+ * groups (G = 0: NVF_LAYOUT_TILED; G >= 1: NVF_LAYOUT_TILED_GROUPED). */
+size_t nvfp4_tiled_bytes(int64_t rows, int32_t G, int32_t K);
 
 /* Per-group global scales gs[g] = amax(x[g]) / 2688 (1 when the group is all
  * zero): x device [groups, n] of dtype x_dtype (NVF_F32 | NVF_BF16), gs_out
@@ -113,16 +127,19 @@ nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, in
  *   rows, K      K a positive multiple of 64; ldx >= K, x 16-byte aligned,
  *                ldx * element size a multiple of 16.
  *   group_offsets device int32[G+1] (nullable): rows [offsets[g], offsets[g+1])
- *                use gscale[g]; required for NVF_SF_GROUPED together with
- *                tile_offsets (device int32[G+1]).  Without offsets gscale[0]
- *                is used for every row.
+ *                use gscale[g]; required for NVF_LAYOUT_TILED_GROUPED together
+ *                with tile_offsets (device int32[G+1]).  Without offsets
+ *                gscale[0] is used for every row.
  *   gscale       device float (see above), finite and > 0.
- *   codes        device uint8[rows, K/2] (16-byte aligned); scales: layout above.
+ *   codes        device, 16-byte aligned: uint8[rows, K/2] for ROWMAJOR, the
+ *                whole tiled buffer for the tiled layouts.
+ *   scales       device uint8[rows, K/16] (4-byte aligned) for ROWMAJOR; unused
+ *                (may be NULL) for the tiled layouts.
  * Each 16-element block: amax (FP32) -> sb = E4M3_rn_sat(amax / (6 gs)) ->
  * r = 1 / (dec(sb) * gs) (0 if that product is 0) -> q = E2M1_rn_sat(x * r). */
 nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t K, int64_t ldx,
                           const int32_t* gather_rows, const int32_t* group_offsets, const int32_t* tile_offsets,
-                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t layout,
                           void* stream);
 
 /* Top-k routing and permutation (steps 1-2).
@@ -172,29 +189,26 @@ nvf_status moe_route_permute_noalloc(const float* logits, const float* bias, int
                                      int32_t* src_to_perm, int32_t* perm_token, void* stream);
 
 /* Grouped block-scaled FP4 GEMM (steps 4 / 6 with a plain epilogue):
- *   D[row, n] = gs_a[g] * gs_b[g] * sum_k A[row, k] B[g, n, k]   for offsets[g] <= row < offsets[g+1].
- *   A       device uint8[a_rows, K/2] codes; a_rows bounds every row the GEMM may
- *           touch (offsets[G] <= a_rows); A_sf NVF_SF_GROUPED scales.
- *   B       device uint8[G, N, K/2]; B_sf NVF_SF_MMA scales of the [G*N, K] matrix.
+ *   D[row, n] = gs_a[g] * gs_b[g] * sum_k A[row, k] B[g*N + n, k]   for offsets[g] <= row < offsets[g+1].
+ *   A       device NVF_LAYOUT_TILED_GROUPED buffer of K columns; a_rows bounds
+ *           the rows (offsets[G] <= a_rows, buffer of nvfp4_tiled_bytes(a_rows, G, K)).
+ *   B       device NVF_LAYOUT_TILED buffer of the [G*N, K] weight matrix.
  *   gs_a, gs_b device float[G]; group_offsets, tile_offsets device int32[G+1].
- *   N a positive multiple of 128, K a positive multiple of 64, K/2 a multiple of 16.
+ *   N a positive multiple of 128, K a positive multiple of 64.
  *   D       device [a_rows, ldd] of out_dtype (NVF_F32 | NVF_BF16); only rows of
  *           groups are written.  ldd * element size a multiple of 16. */
-nvf_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
-                              const uint8_t* B_sf, const float* gs_a, const float* gs_b, const int32_t* group_offsets,
-                              const int32_t* tile_offsets, int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D,
-                              int64_t ldd, void* stream);
+nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B, const float* gs_a,
+                              const float* gs_b, const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G,
+                              int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream);
 
 /* Prepared expert weights (all device pointers). */
 typedef struct nvf_moe_weights {
   int32_t E;               /* routed experts */
   int32_t H, I;            /* hidden, intermediate: multiples of 128 and 64 */
   int32_t shared;          /* 1: expert E is an always-on shared expert */
-  const uint8_t* w13;      /* uint8[E', 2I, H/2], rows in nvf_w13_row_map order */
-  const uint8_t* w13_sf;   /* NVF_SF_MMA scales of [E'*2I, H] */
+  const uint8_t* w13;      /* NVF_LAYOUT_TILED [E'*2I, H], rows of each expert in nvf_w13_row_map order */
   const float* gs_w13;     /* float[E'] */
-  const uint8_t* w2;       /* uint8[E', H, I/2] */
-  const uint8_t* w2_sf;    /* NVF_SF_MMA scales of [E'*H, I] */
+  const uint8_t* w2;       /* NVF_LAYOUT_TILED [E'*H, I] */
   const float* gs_w2;      /* float[E'] */
 } nvf_moe_weights;
 
@@ -202,9 +216,12 @@ typedef struct nvf_moe_weights {
  * (debug and test access; layouts as documented above). */
 typedef struct nvf_moe_ws_layout {
   size_t topk_ids, topk_w, expert_offsets, tile_offsets, perm_to_src, src_to_perm, perm_token;
-  size_t a1_codes, a1_sf, a2_codes, a2_sf, y;  /* y: float[R, H] */
-  size_t route_scratch, total;
-  int64_t R;                                   /* rows after permutation */
+  size_t route_scratch;
+  size_t a1;                /* NVF_LAYOUT_TILED_GROUPED, K = H */
+  size_t a2;                /* NVF_LAYOUT_TILED_GROUPED, K = I */
+  size_t y;                 /* float[R, H], row = permuted slot */
+  size_t total;
+  int64_t R;                /* rows after permutation */
 } nvf_moe_ws_layout;
 
 nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I, int32_t k, int32_t shared,
@@ -218,7 +235,9 @@ nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I
  *   ws       device scratch of nvfp4_moe_workspace_layout().total bytes, 256-byte aligned.
  *   stage_events NULL, or NVF_MOE_STAGE_EVENTS cudaEvent_t handles recorded on `stream`
  *            before routing and after each stage (route+permute, activation quant,
- *            gate_up GEMM, down GEMM, combine), for per-stage timing. */
+ *            gate_up GEMM, down GEMM, combine), for per-stage timing; small
+ *            batches route and quantize in one kernel, and then the events
+ *            after routing and after quantization are recorded together. */
 #define NVF_MOE_STAGE_EVENTS 6
 nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
                              int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,

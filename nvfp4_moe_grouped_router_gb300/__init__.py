@@ -17,7 +17,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
 
 NVF_F32, NVF_BF16 = 0, 1
-SF_ROWMAJOR, SF_MMA, SF_GROUPED = 0, 1, 2
+LAYOUT_ROWMAJOR, LAYOUT_TILED, LAYOUT_TILED_GROUPED = 0, 1, 2
+TILE_BYTES = 18432   # one (128-row, 256-K) chunk: 16 KB swizzled codes + 2 KB scale atoms
 STATUS = {0: "NVF_OK", 1: "NVF_ERR_INVALID_ARG", 2: "NVF_ERR_UNSUPPORTED_DEVICE", 3: "NVF_ERR_WORKSPACE",
           4: "NVF_ERR_CUDA", 5: "NVF_ERR_TIMEOUT", 6: "NVF_ERR_DEVICE_CHECK"}
 
@@ -29,14 +30,13 @@ SIGNATURES = {
     "nvf_abi_version": (_I32, []),
     "nvf_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "nvf_w13_row_map": (ctypes.c_int, [_I32, ctypes.POINTER(_I32)]),
-    "nvfp4_grouped_scale_bytes": (_SZ, [_I64, _I32, _I32]),
+    "nvfp4_tiled_bytes": (_SZ, [_I64, _I32, _I32]),
     "nvfp4_global_scale": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I32, _I64, _I32, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _P]),
     "moe_route_permute_workspace_size": (ctypes.c_int, [_I32, _I32, ctypes.POINTER(_SZ)]),
     "moe_route_permute": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                          _SZ, _P]),
-    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
-                                          _P]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P]),
     "nvfp4_moe_workspace_layout": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "moe_route_permute_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                                  _P]),
@@ -52,14 +52,14 @@ class NvfError(RuntimeError):
 
 
 class MoEWeightsC(ctypes.Structure):
-    _fields_ = [("E", _I32), ("H", _I32), ("I", _I32), ("shared", _I32), ("w13", _P), ("w13_sf", _P),
-                ("gs_w13", _P), ("w2", _P), ("w2_sf", _P), ("gs_w2", _P)]
+    _fields_ = [("E", _I32), ("H", _I32), ("I", _I32), ("shared", _I32), ("w13", _P), ("gs_w13", _P),
+                ("w2", _P), ("gs_w2", _P)]
 
 
 class WorkspaceLayoutC(ctypes.Structure):
     _fields_ = [(n, _SZ) for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src",
-                                    "src_to_perm", "perm_token", "a1_codes", "a1_sf", "a2_codes", "a2_sf", "y",
-                                    "route_scratch", "total")] + [("R", _I64)]
+                                    "src_to_perm", "perm_token", "route_scratch", "a1", "a2", "y",
+                                    "total")] + [("R", _I64)]
 
 
 _lib = None
@@ -122,12 +122,9 @@ def w13_row_map(I: int):
     return list(m)
 
 
-def grouped_scale_bytes(rows: int, G: int, K: int) -> int:
-    return int(lib().nvfp4_grouped_scale_bytes(rows, G, K))
-
-
-def mma_scale_bytes(rows: int, K: int) -> int:
-    return (rows + 127) // 128 * 128 * (K // 16)
+def tiled_bytes(rows: int, G: int, K: int) -> int:
+    """Bytes of a tiled operand (G = 0: TILED, G >= 1: TILED_GROUPED)."""
+    return int(lib().nvfp4_tiled_bytes(rows, G, K))
 
 
 # ----------------------------------------------------------------------------- entry points
@@ -139,19 +136,24 @@ def global_scale(x: torch.Tensor, groups: int = 1) -> torch.Tensor:
     return gs
 
 
-def quantize(x: torch.Tensor, gscale: torch.Tensor, layout: int = SF_ROWMAJOR, gather=None, offsets=None,
+def quantize(x: torch.Tensor, gscale: torch.Tensor, layout: int = LAYOUT_ROWMAJOR, gather=None, offsets=None,
              tile_offsets=None, rows=None, codes=None, scales=None):
-    """NVFP4 codes [rows, K/2] and scales (layout) of the rows of a 2-D tensor x."""
+    """NVFP4 quantization of the rows of a 2-D tensor x.
+
+    ROWMAJOR: returns (codes [rows, K/2], scales [rows, K/16]); tiled layouts:
+    returns (buffer, None)."""
     _cuda(x, "x")
     K = x.shape[1]
     rows = (gather.numel() if gather is not None else x.shape[0]) if rows is None else rows
     G = offsets.numel() - 1 if offsets is not None else 1
     if codes is None:
-        codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
-    if scales is None:
-        n = {SF_ROWMAJOR: rows * (K // 16), SF_MMA: mma_scale_bytes(rows, K),
-             SF_GROUPED: grouped_scale_bytes(rows, G, K)}[layout]
-        scales = torch.zeros(max(n, 16), dtype=torch.uint8, device=x.device)
+        if layout == LAYOUT_ROWMAJOR:
+            codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+        else:
+            codes = torch.zeros(max(tiled_bytes(rows, G if layout == LAYOUT_TILED_GROUPED else 0, K), 16),
+                                dtype=torch.uint8, device=x.device)
+    if scales is None and layout == LAYOUT_ROWMAJOR:
+        scales = torch.empty(max(rows * (K // 16), 16), dtype=torch.uint8, device=x.device)
     _check(lib().nvfp4_quantize(_ptr(x), _dtype_code(x), rows, K, x.stride(0), _ptr(gather), _ptr(offsets),
                                 _ptr(tile_offsets), G, _ptr(gscale), _ptr(codes), _ptr(scales), layout, _stream()))
     return codes, scales
@@ -181,17 +183,18 @@ def route_permute(logits: torch.Tensor, k: int, bias=None, renormalize=True, sha
     return out
 
 
-def grouped_gemm(A, A_sf, B, B_sf, gs_a, gs_b, offsets, tile_offsets, N: int, K: int, out_dtype=torch.float32,
+def grouped_gemm(A, a_rows: int, B, gs_a, gs_b, offsets, tile_offsets, N: int, K: int, out_dtype=torch.float32,
                  D=None):
-    """D[row] = gs_a[g] gs_b[g] A[row] . B[g]^T for the rows of group g (rows of A beyond offsets[G] untouched)."""
-    a_rows = A.shape[0]
+    """D[row] = gs_a[g] gs_b[g] A[row] . B[g]^T for the rows of group g.
+
+    A: TILED_GROUPED buffer (K columns, up to a_rows rows); B: TILED buffer of the
+    [G*N, K] weights.  Rows of D outside the groups are left untouched."""
     G = offsets.numel() - 1
     if D is None:
-        D = torch.zeros(a_rows, N, dtype=out_dtype, device=A.device)
+        D = torch.zeros(max(a_rows, 1), N, dtype=out_dtype, device=A.device)
     code = NVF_F32 if D.dtype == torch.float32 else NVF_BF16
-    _check(lib().nvfp4_grouped_gemm(_ptr(A), _ptr(A_sf), a_rows, _ptr(B), _ptr(B_sf), _ptr(gs_a), _ptr(gs_b),
-                                    _ptr(offsets), _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0),
-                                    _stream()))
+    _check(lib().nvfp4_grouped_gemm(_ptr(A), a_rows, _ptr(B), _ptr(gs_a), _ptr(gs_b), _ptr(offsets),
+                                    _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0), _stream()))
     return D
 
 
@@ -202,17 +205,14 @@ class MoEWeights:
     H: int
     I: int
     shared: bool
-    w13: torch.Tensor     # uint8 [E', 2I, H/2], prepared row order
-    w13_sf: torch.Tensor  # MMA-layout scales
+    w13: torch.Tensor     # TILED [E'*2I, H], prepared row order (w13_row_map)
     gs_w13: torch.Tensor  # float [E']
-    w2: torch.Tensor      # uint8 [E', H, I/2]
-    w2_sf: torch.Tensor
+    w2: torch.Tensor      # TILED [E'*H, I]
     gs_w2: torch.Tensor
 
     def c_struct(self) -> MoEWeightsC:
-        return MoEWeightsC(self.E, self.H, self.I, int(self.shared), self.w13.data_ptr(), self.w13_sf.data_ptr(),
-                           self.gs_w13.data_ptr(), self.w2.data_ptr(), self.w2_sf.data_ptr(),
-                           self.gs_w2.data_ptr())
+        return MoEWeightsC(self.E, self.H, self.I, int(self.shared), self.w13.data_ptr(), self.gs_w13.data_ptr(),
+                           self.w2.data_ptr(), self.gs_w2.data_ptr())
 
 
 def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="cuda") -> MoEWeights:
@@ -220,17 +220,15 @@ def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="c
 
     expert_fp32(e) -> (w13 [2I, H], w2 [H, I]) float32 tensors on `device` (gate rows
     first, then up rows).  Per expert: gs = amax / 2688, NVFP4 rows along the
-    input dimension, w13 rows reordered by w13_row_map, scales in MMA layout.
+    input dimension, w13 rows reordered by w13_row_map, TILED layout.
     """
     Et = E + int(shared)
-    w13 = torch.empty(Et, 2 * I, H // 2, dtype=torch.uint8, device=device)
-    w13_sf = torch.empty(Et * 2 * I * H // 16, dtype=torch.uint8, device=device)
-    w2 = torch.empty(Et, H, I // 2, dtype=torch.uint8, device=device)
-    w2_sf = torch.empty(Et * H * I // 16, dtype=torch.uint8, device=device)
+    n13, n2 = tiled_bytes(2 * I, 0, H), tiled_bytes(H, 0, I)     # one expert's chunks
+    w13 = torch.zeros(Et * n13, dtype=torch.uint8, device=device)
+    w2 = torch.zeros(Et * n2, dtype=torch.uint8, device=device)
     gs13 = torch.empty(Et, dtype=torch.float32, device=device)
     gs2 = torch.empty(Et, dtype=torch.float32, device=device)
     rmap = torch.tensor(w13_row_map(I), dtype=torch.int32, device=device)
-    n13, n2 = 2 * I * H // 16, H * I // 16
     for e in range(Et):
         a, b = expert_fp32(e)
         a = a.to(device=device, dtype=torch.float32).contiguous()
@@ -239,9 +237,9 @@ def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="c
         g2 = global_scale(b)
         gs13[e:e + 1].copy_(g13)
         gs2[e:e + 1].copy_(g2)
-        quantize(a, g13, SF_MMA, gather=rmap, codes=w13[e], scales=w13_sf[e * n13:(e + 1) * n13])
-        quantize(b, g2, SF_MMA, codes=w2[e], scales=w2_sf[e * n2:(e + 1) * n2])
-    return MoEWeights(E, H, I, shared, w13, w13_sf, gs13, w2, w2_sf, gs2)
+        quantize(a, g13, LAYOUT_TILED, gather=rmap, codes=w13[e * n13:(e + 1) * n13])
+        quantize(b, g2, LAYOUT_TILED, codes=w2[e * n2:(e + 1) * n2])
+    return MoEWeights(E, H, I, shared, w13, gs13, w2, gs2)
 
 
 def workspace_layout(T: int, E: int, H: int, I: int, k: int, shared: bool) -> dict:

@@ -2,6 +2,7 @@
 // launch sequence.  See include/nvfp4moe.h for the contract of every entry point.
 #include "../../include/nvfp4moe.h"
 #include "internal.h"
+#include "layout.cuh"
 #include "ptx.cuh"
 
 #include <cstdarg>
@@ -150,9 +151,9 @@ nvf_status nvf_w13_row_map(int32_t I, int32_t* map) {
   return NVF_OK;
 }
 
-size_t nvfp4_grouped_scale_bytes(int64_t rows, int32_t G, int32_t K) {
+size_t nvfp4_tiled_bytes(int64_t rows, int32_t G, int32_t K) {
   if (rows < 0 || G < 0 || K <= 0) return 0;
-  return static_cast<size_t>((rows + 127) / 128 + G) * 128 * static_cast<size_t>(K / 16);
+  return static_cast<size_t>((rows + 127) / 128 + G) * num_k_tiles(K) * TILE_BYTES;
 }
 
 nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, int64_t n, float* gs_out,
@@ -168,10 +169,12 @@ nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, in
 
 nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t K, int64_t ldx,
                           const int32_t* gather_rows, const int32_t* group_offsets, const int32_t* tile_offsets,
-                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                          int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t layout,
                           void* stream) {
   NVF_BEGIN();
-  NVF_REQUIRE(x && gscale && codes && scales, "x, gscale, codes and scales must not be NULL");
+  NVF_REQUIRE(layout >= NVF_LAYOUT_ROWMAJOR && layout <= NVF_LAYOUT_TILED_GROUPED, "bad layout %d", layout);
+  NVF_REQUIRE(x && gscale && codes && (scales || layout != NVF_LAYOUT_ROWMAJOR),
+              "x, gscale, codes (and scales for NVF_LAYOUT_ROWMAJOR) must not be NULL");
   NVF_REQUIRE(x_dtype == NVF_F32 || x_dtype == NVF_BF16, "x_dtype=%d must be NVF_F32 or NVF_BF16", x_dtype);
   NVF_REQUIRE(rows >= 0 && K > 0 && K % 64 == 0, "rows=%lld K=%d: K must be a positive multiple of 64",
               (long long)rows, K);
@@ -180,12 +183,11 @@ nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t 
   NVF_REQUIRE(aligned16(x) && (ldx * esz) % 16 == 0, "x must be 16-byte aligned with a 16-byte multiple row pitch");
   NVF_REQUIRE(aligned16(codes) && (reinterpret_cast<uintptr_t>(scales) & 3u) == 0,
               "codes must be 16-byte and scales 4-byte aligned");
-  NVF_REQUIRE(scale_layout >= NVF_SF_ROWMAJOR && scale_layout <= NVF_SF_GROUPED, "bad scale_layout %d", scale_layout);
   if (group_offsets) NVF_REQUIRE(G >= 1, "G=%d must be >= 1 with group_offsets", G);
-  if (scale_layout == NVF_SF_GROUPED)
-    NVF_REQUIRE(group_offsets && tile_offsets, "NVF_SF_GROUPED needs group_offsets and tile_offsets");
+  if (layout == NVF_LAYOUT_TILED_GROUPED)
+    NVF_REQUIRE(group_offsets && tile_offsets, "NVF_LAYOUT_TILED_GROUPED needs group_offsets and tile_offsets");
   QuantArgs a{x, x_dtype, rows, K, ldx, gather_rows, group_offsets, tile_offsets, group_offsets ? G : 1,
-              gscale, codes, scales, scale_layout};
+              gscale, codes, scales, layout};
   NVF_CUDA(launch_quantize(a, static_cast<cudaStream_t>(stream)), "quantize launch");
   return NVF_OK;
 }
@@ -232,26 +234,24 @@ nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, 
   return NVF_OK;
 }
 
-static nvf_status validate_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
-                                const uint8_t* B_sf, int32_t G, int32_t N, int32_t K) {
-  NVF_REQUIRE(A && A_sf && B && B_sf, "A, A_sf, B and B_sf must not be NULL");
+static nvf_status validate_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B, int32_t G, int32_t N,
+                                int32_t K) {
+  NVF_REQUIRE(A && B, "A and B must not be NULL");
   NVF_REQUIRE(G >= 1 && G <= 4096, "G=%d must be in [1, 4096]", G);
   NVF_REQUIRE(N > 0 && N % 128 == 0, "N=%d must be a positive multiple of 128", N);
   NVF_REQUIRE(K > 0 && K % 64 == 0, "K=%d must be a positive multiple of 64", K);
   NVF_REQUIRE(a_rows >= 0 && a_rows < (int64_t(1) << 31), "a_rows=%lld out of range", (long long)a_rows);
   NVF_REQUIRE(static_cast<int64_t>(G) * N < (int64_t(1) << 31), "G*N overflows int32");
-  NVF_REQUIRE(aligned16(A) && aligned16(B) && aligned16(A_sf) && aligned16(B_sf),
-              "A, B, A_sf and B_sf must be 16-byte aligned");
+  NVF_REQUIRE(aligned16(A) && aligned16(B), "A and B must be 16-byte aligned");
   return NVF_OK;
 }
 
-nvf_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_rows, const uint8_t* B,
-                              const uint8_t* B_sf, const float* gs_a, const float* gs_b, const int32_t* group_offsets,
-                              const int32_t* tile_offsets, int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D,
-                              int64_t ldd, void* stream) {
+nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B, const float* gs_a,
+                              const float* gs_b, const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G,
+                              int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream) {
   NVF_BEGIN();
   {
-    nvf_status s = validate_gemm(A, A_sf, a_rows, B, B_sf, G, N, K);
+    nvf_status s = validate_gemm(A, a_rows, B, G, N, K);
     if (s != NVF_OK) return s;
   }
   NVF_REQUIRE(gs_a && gs_b && group_offsets && tile_offsets && D, "gs_a, gs_b, offsets and D must not be NULL");
@@ -261,7 +261,7 @@ nvf_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* A_sf, int64_t a_r
               "D must be 16-byte aligned with ldd >= N=%d and ldd*%d bytes a multiple of 16 (ldd=%lld)", N, esz,
               (long long)ldd);
   GemmArgs a{};
-  a.a = A; a.a_rows = a_rows; a.a_sf = A_sf; a.b = B; a.b_sf = B_sf; a.gs_a = gs_a; a.gs_b = gs_b;
+  a.a = A; a.a_rows = a_rows; a.b = B; a.gs_a = gs_a; a.gs_b = gs_b;
   a.offsets = group_offsets; a.tile_offs = tile_offsets; a.G = G; a.N = N; a.K = K;
   a.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
   a.d = D; a.ldd = ldd; a.err = dev_->err;
@@ -302,10 +302,8 @@ nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I
   size_t rs = 0;
   moe_route_permute_workspace_size(T, E, &rs);
   L->route_scratch = take(rs);
-  L->a1_codes = take(static_cast<size_t>(R) * H / 2);
-  L->a1_sf = take(nvfp4_grouped_scale_bytes(R, static_cast<int32_t>(Et), H));
-  L->a2_codes = take(static_cast<size_t>(R) * I / 2);
-  L->a2_sf = take(nvfp4_grouped_scale_bytes(R, static_cast<int32_t>(Et), I));
+  L->a1 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), H));
+  L->a2 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), I));
   L->y = take(sizeof(float) * static_cast<size_t>(R) * H);
   L->total = off;
   return NVF_OK;
@@ -323,9 +321,8 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
     if (s != NVF_OK) return s;
   }
   const int32_t E = w->E, H = w->H, I = w->I, Et = w->E + w->shared;
-  NVF_REQUIRE(w->w13 && w->w13_sf && w->gs_w13 && w->w2 && w->w2_sf && w->gs_w2, "weight pointers must not be NULL");
-  NVF_REQUIRE(aligned16(w->w13) && aligned16(w->w2) && aligned16(w->w13_sf) && aligned16(w->w2_sf),
-              "weight buffers must be 16-byte aligned");
+  NVF_REQUIRE(w->w13 && w->gs_w13 && w->w2 && w->gs_w2, "weight pointers must not be NULL");
+  NVF_REQUIRE(aligned16(w->w13) && aligned16(w->w2), "weight buffers must be 16-byte aligned");
   NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
   if (T == 0) return NVF_OK;
   NVF_REQUIRE(x && logits && gs_a1 && gs_a2 && out, "x, logits, gs_a1, gs_a2 and out must not be NULL");
@@ -354,16 +351,16 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   NVF_CUDA(mark(1), "cudaEventRecord");
 
   QuantArgs qa{x, NVF_BF16, L.R, H, H, i32(L.perm_token), i32(L.expert_offsets), i32(L.tile_offsets), Et,
-               gs_a1, base + L.a1_codes, base + L.a1_sf, NVF_SF_GROUPED};
+               gs_a1, base + L.a1, nullptr, NVF_LAYOUT_TILED_GROUPED};
   NVF_CUDA(launch_quantize(qa, s), "activation quantize launch");
   NVF_CUDA(mark(2), "cudaEventRecord");
 
   const char* why = nullptr;
   GemmArgs g1{};
-  g1.a = base + L.a1_codes; g1.a_rows = L.R; g1.a_sf = base + L.a1_sf;
-  g1.b = w->w13; g1.b_sf = w->w13_sf; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
+  g1.a = base + L.a1; g1.a_rows = L.R;
+  g1.b = w->w13; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
   g1.offsets = i32(L.expert_offsets); g1.tile_offs = i32(L.tile_offsets); g1.G = Et; g1.N = 2 * I; g1.K = H;
-  g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2_codes; g1.q_sf = base + L.a2_sf; g1.gs_q = gs_a2;
+  g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2; g1.gs_q = gs_a2;
   g1.h_dump = h_dump; g1.err = dev_->err;
   cudaError_t e = launch_grouped_gemm(g1, s, &why);
   if (e != cudaSuccess)
@@ -372,8 +369,8 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   NVF_CUDA(mark(3), "cudaEventRecord");
 
   GemmArgs g2{};
-  g2.a = base + L.a2_codes; g2.a_rows = L.R; g2.a_sf = base + L.a2_sf;
-  g2.b = w->w2; g2.b_sf = w->w2_sf; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
+  g2.a = base + L.a2; g2.a_rows = L.R;
+  g2.b = w->w2; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
   g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
   e = launch_grouped_gemm(g2, s, &why);

@@ -8,17 +8,21 @@
 // "Purpose": nvfp4_blockwise_moe_kernel.cu) with a per-expert alpha and beta = 0
 // (vLLM PR #29242 review: alpha_ptr_array, beta = 0.0f).
 //
-// Design (one CTA per SM, persistent, 192 threads):
-//   warp 0   TMA producer: 128x256 (rows x K) FP4 tiles of A and B with 128-byte
-//            swizzle, plus the four 512-byte scale atoms of each, into a
-//            STAGES-deep shared-memory ring (mbarrier full/empty pairs).
-//   warp 1   TMEM owner and MMA issuer: per stage, tcgen05.cp the scale atoms
-//            into TMEM, then four 128x128x64 block-scaled MMAs into one of two
-//            FP32 TMEM accumulators (128 columns each).
-//   warps 2-5 epilogue: tcgen05.ld the accumulator (one 32-lane quarter per
-//            warp), scale by alpha and either store FP32/BF16 rows or compute
-//            h = silu(gate) * up and requantize it to NVFP4 (codes + scale
-//            atoms for the next GEMM).
+// Design (one CTA per SM, persistent, 320 threads):
+//   warp 0    producer: per pipeline stage one contiguous 18 KB chunk of B
+//             (128 weight rows x 256 K, codes pre-swizzled + scale atoms) and
+//             the valid-row prefix of the matching A chunk, moved with 1-D
+//             bulk copies (cp.async.bulk) into a STAGES-deep ring guarded by
+//             mbarrier full/empty pairs.  Weights therefore stream from HBM as
+//             sequential 18 KB runs.
+//   warp 1    TMEM owner and MMA issuer: per stage, tcgen05.cp the scale atoms
+//             into TMEM, then four 128x128x64 block-scaled MMAs into one of two
+//             FP32 TMEM accumulators (128 columns each).
+//   warps 2-9 epilogue: two warps per 32-lane TMEM quarter, 64 columns each;
+//             tcgen05.ld, scale by alpha, then either store FP32/BF16 rows or
+//             compute h = silu(gate) * up and requantize it to NVFP4 straight
+//             into the next GEMM's tiled operand.  Warps whose 32 rows are all
+//             past the group's end skip the arithmetic.
 // Tiles are 128 rows of one group x 128 output columns; the scheduler walks
 // (m-tile, n-tile) pairs with the m-tile index taken from the device-side
 // tile prefix, so no host synchronisation is needed for group sizes.
@@ -30,35 +34,30 @@
 #include "quant_block.cuh"
 
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 namespace nvf {
 namespace {
 
 constexpr int BM = 128;             // rows of A per tile (MMA M)
 constexpr int BN = 128;             // output columns per tile (MMA N)
-constexpr int BKB = 128;            // K bytes per stage (256 FP4 values)
-constexpr int STAGES = 5;
-constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
-constexpr int SF_BYTES = 4 * 512;   // four 512-byte atoms (K = 4 x 64)
-constexpr int THREADS = 192;
+#ifndef NVF_GEMM_STAGES
+#define NVF_GEMM_STAGES 5
+#endif
+constexpr int STAGES = NVF_GEMM_STAGES;
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // A chunk + B chunk
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 2 * BN;  // accumulators use columns [0, 256)
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
+constexpr int OFF_BAR = STAGES * STAGE_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 
 static_assert(SF_COL0 + STAGES * 32 <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(TILE_BYTES % 1024 == 0, "B chunk must stay 1024-byte aligned in shared memory");
 
 struct Tile {
   int g, mt, nt, row0, rows;
@@ -89,9 +88,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs p) {
+__global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_addr(smem);
@@ -100,6 +97,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  auto stage_a = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
+  auto stage_b = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES + TILE_BYTES); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
@@ -112,13 +111,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);
+      mbar_init(acce_bar(b), EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
   tc_fence_before();
@@ -140,19 +137,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile x = decode_tile(t, p, ntiles);
-        const uint8_t* sfa = p.a_sf + static_cast<size_t>(x.mt) * k64 * 512;
-        const uint8_t* sfb = p.b_sf + (static_cast<size_t>(x.g) * ntiles + x.nt) * k64 * 512;
+        const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
+        const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt) * nkt * TILE_BYTES;
+        // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
+        const uint32_t a_code_bytes = static_cast<uint32_t>(min(BM, (x.rows + 7) & ~7)) * 128u;
         for (int kt = 0; kt < nkt; ++kt) {
           if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
             ok = false;
             break;
           }
-          const int na = min(4, k64 - kt * 4);
-          mbar_arrive_expect_tx(full_bar(stage), A_BYTES + B_BYTES + 2 * na * 512);
-          tma_load_2d(s_base + OFF_A + stage * A_BYTES, &tmA, kt * BKB, x.row0, full_bar(stage));
-          tma_load_2d(s_base + OFF_B + stage * B_BYTES, &tmB, kt * BKB, x.g * p.N + x.nt * BN, full_bar(stage));
-          bulk_load(s_base + OFF_SFA + stage * SF_BYTES, sfa + kt * 4 * 512, na * 512, full_bar(stage));
-          bulk_load(s_base + OFF_SFB + stage * SF_BYTES, sfb + kt * 4 * 512, na * 512, full_bar(stage));
+          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + TILE_SF_BYTES + TILE_BYTES);
+          const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
+          if (a_code_bytes == TILE_CODE_BYTES) {
+            bulk_load(stage_a(stage), ac, TILE_BYTES, full_bar(stage));
+          } else {
+            bulk_load(stage_a(stage), ac, a_code_bytes, full_bar(stage));
+            bulk_load(stage_a(stage) + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
+          }
+          bulk_load(stage_b(stage), b_chunk + static_cast<size_t>(kt) * TILE_BYTES, TILE_BYTES, full_bar(stage));
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
           if (++stage == STAGES) {
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok || *abort_flag) {
-        // Let every load this thread issued land before the CTA goes away.
+        // Let every copy this thread issued land before the CTA goes away.
         for (int s = 0; s < STAGES; ++s)
           if ((pending >> s) & 1u) mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
       }
@@ -189,14 +191,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int na = min(4, k64 - kt * 4);
           const uint32_t sfa_t = tmem + SF_COL0 + stage * 32;
           const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t sa = s_base + OFF_SFA + stage * SF_BYTES;
-          const uint32_t sb = s_base + OFF_SFB + stage * SF_BYTES;
+          const uint32_t a_s = stage_a(stage), b_s = stage_b(stage);
           for (int kk = 0; kk < na; ++kk) {
-            tc_copy_sf_atom(sfa_t + kk * 4, sf_atom_desc(sa + kk * 512));
-            tc_copy_sf_atom(sfb_t + kk * 4, sf_atom_desc(sb + kk * 512));
+            tc_copy_sf_atom(sfa_t + kk * 4, sf_atom_desc(a_s + TILE_CODE_BYTES + kk * 512));
+            tc_copy_sf_atom(sfb_t + kk * 4, sf_atom_desc(b_s + TILE_CODE_BYTES + kk * 512));
           }
-          const uint32_t a_s = s_base + OFF_A + stage * A_BYTES;
-          const uint32_t b_s = s_base + OFF_B + stage * B_BYTES;
           for (int kk = 0; kk < na; ++kk) {
             tc_mma_nvfp4(d_tmem, operand_desc_sw128(a_s + kk * 32), operand_desc_sw128(b_s + kk * 32), idesc,
                          sfa_t + kk * 4, sfb_t + kk * 4, (kt | kk) != 0 ? 1u : 0u);
@@ -215,80 +214,86 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;      // tile row handled by this thread
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;       // which 64 of the tile's 128 columns
+    const int r = q * 32 + lane;            // tile row handled by this thread
     int i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const Tile x = decode_tile(t, p, ntiles);
       const int buf = i & 1;
       if (!mbar_wait(accf_bar(buf), (i >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_EPILOGUE, t)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + buf * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const float alpha = __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g));
-      const bool valid = r < x.rows;
-      const int64_t row = static_cast<int64_t>(x.row0) + r;
-      if constexpr (EPI == EPI_SWIGLU_QUANT) {
-        const int I = p.N >> 1;
-        const float gsq = __ldg(p.gs_q + x.g);
-        const float six_gsq = __fmul_rn(6.0f, gsq);
-        uint32_t cw[8];
-        uint32_t sfw = 0;
+      if (q * 32 < x.rows) {
+        const uint32_t tb = tmem + buf * BN + half * 64 + (static_cast<uint32_t>(q * 32) << 16);
+        const float alpha = __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g));
+        const bool valid = r < x.rows;
+        const int64_t row = static_cast<int64_t>(x.row0) + r;
+        if constexpr (EPI == EPI_SWIGLU_QUANT) {
+          const int I = p.N >> 1;
+          const float gsq = __ldg(p.gs_q + x.g);
+          const float six_gsq = __fmul_rn(6.0f, gsq);
+          uint32_t cw[4];
+          uint32_t sfw = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_ld_wait();
-          float h[16];
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tb + cc * 32, v);
+            tmem_ld_wait();
+            float h[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g = __fmul_rn(__uint_as_float(v[j]), alpha);
-            const float u = __fmul_rn(__uint_as_float(v[16 + j]), alpha);
-            h[j] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+            for (int j = 0; j < 16; ++j) {
+              // rows past the group's end carry whatever their scale bytes held: use zeros
+              const float g = valid ? __fmul_rn(__uint_as_float(v[j]), alpha) : 0.0f;
+              const float u = valid ? __fmul_rn(__uint_as_float(v[16 + j]), alpha) : 0.0f;
+              h[j] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
+            }
+            const int c = half * 2 + cc;   // 16-wide block of this n-tile's 64 h values
+            if (p.h_dump != nullptr && valid) {
+              float4* hd = reinterpret_cast<float4*>(p.h_dump + row * I + x.nt * 64 + c * 16);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+            }
+            sfw |= quant_block16(h, gsq, six_gsq, cw[2 * cc], cw[2 * cc + 1]) << (8 * cc);
           }
-          if (p.h_dump != nullptr && valid) {
-            float4* hd = reinterpret_cast<float4*>(p.h_dump + row * I + x.nt * 64 + c * 16);
+          // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): this n-tile's 64
+          // h values are MMA step nt % 4 of K tile nt / 4; this warp's 32 of them
+          // are one 16-byte code chunk and two scale bytes of row r.
+          uint8_t* chunk = p.q_codes + (static_cast<size_t>(x.mt) * num_k_tiles(I) + (x.nt >> 2)) * TILE_BYTES;
+          if (valid)
+            *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, (x.nt & 3) * 32 + half * 16)) =
+                make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint16_t*>(chunk + TILE_CODE_BYTES + (x.nt & 3) * 512 +
+                                       sf_atom_offset(static_cast<uint32_t>(r), half * 2)) =
+              static_cast<uint16_t>(sfw);
+        } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-          }
-          sfw |= quant_block16(h, gsq, six_gsq, cw[2 * c], cw[2 * c + 1]) << (8 * c);
-        }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.q_codes + row * (I >> 1) + x.nt * 32);
-          dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        }
-        // Scale atoms of this tile belong to it alone: rows past the group end
-        // are written too (never read as valid data).
-        *reinterpret_cast<uint32_t*>(p.q_sf + (static_cast<size_t>(x.mt) * (I >> 6) + x.nt) * 512 +
-                                     sf_atom_offset(static_cast<uint32_t>(r), 0)) = sfw;
-      } else {
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tb + cc * 32, v);
+            tmem_ld_wait();
+            if (valid) {
+              const int64_t col = static_cast<int64_t>(x.nt) * BN + half * 64 + cc * 32;
+              if constexpr (EPI == EPI_STORE_F32) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.ldd + col);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_ld_wait();
-          if (valid) {
-            const int64_t col = static_cast<int64_t>(x.nt) * BN + c * 32;
-            if constexpr (EPI == EPI_STORE_F32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.ldd + col);
+                for (int j = 0; j < 8; ++j)
+                  dst[j] = make_float4(__fmul_rn(__uint_as_float(v[4 * j]), alpha),
+                                       __fmul_rn(__uint_as_float(v[4 * j + 1]), alpha),
+                                       __fmul_rn(__uint_as_float(v[4 * j + 2]), alpha),
+                                       __fmul_rn(__uint_as_float(v[4 * j + 3]), alpha));
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__fmul_rn(__uint_as_float(v[4 * j]), alpha),
-                                     __fmul_rn(__uint_as_float(v[4 * j + 1]), alpha),
-                                     __fmul_rn(__uint_as_float(v[4 * j + 2]), alpha),
-                                     __fmul_rn(__uint_as_float(v[4 * j + 3]), alpha));
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t w[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t w[4];
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                  __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * j + 2 * h2]), alpha),
-                                                           __fmul_rn(__uint_as_float(v[8 * j + 2 * h2 + 1]), alpha));
-                  w[h2] = *reinterpret_cast<uint32_t*>(&b);
+                  for (int h2 = 0; h2 < 4; ++h2) {
+                    __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * j + 2 * h2]), alpha),
+                                                             __fmul_rn(__uint_as_float(v[8 * j + 2 * h2 + 1]), alpha));
+                    w[h2] = *reinterpret_cast<uint32_t*>(&b);
+                  }
+                  dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
           }
@@ -306,39 +311,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// 2-D byte tensor [rows, cols] (row pitch = cols) loaded in 128 x 128-byte boxes
-// with 128-byte swizzle; rows / columns past the end read as zero.
-bool encode_operand_map(CUtensorMap* m, const void* base, uint64_t cols_bytes, uint64_t rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {cols_bytes, rows};
-  cuuint64_t strides[1] = {cols_bytes};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BKB), static_cast<cuuint32_t>(BM)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI>
-cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
   auto k = grouped_gemm_kernel<EPI>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k<<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, a);
+  k<<<grid, THREADS, SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -347,20 +325,14 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** why) {
   *why = nullptr;
   if (a.a_rows <= 0) return cudaSuccess;
-  CUtensorMap ta, tb;
-  if (!encode_operand_map(&ta, a.a, static_cast<uint64_t>(a.K) / 2, static_cast<uint64_t>(a.a_rows)) ||
-      !encode_operand_map(&tb, a.b, static_cast<uint64_t>(a.K) / 2, static_cast<uint64_t>(a.G) * a.N)) {
-    *why = "cuTensorMapEncodeTiled rejected an operand (alignment / size)";
-    return cudaErrorInvalidValue;
-  }
   const int64_t max_tiles = ((a.a_rows + BM - 1) / BM + a.G) * (a.N / BN);
   int grid = a.max_ctas > 0 ? a.max_ctas : sm_count();
   if (grid > max_tiles) grid = static_cast<int>(max_tiles);
   if (grid < 1) grid = 1;
   switch (a.epilogue) {
-    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(ta, tb, a, grid, s);
-    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(ta, tb, a, grid, s);
-    case EPI_SWIGLU_QUANT: return launch_epi<EPI_SWIGLU_QUANT>(ta, tb, a, grid, s);
+    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(a, grid, s);
+    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(a, grid, s);
+    case EPI_SWIGLU_QUANT: return launch_epi<EPI_SWIGLU_QUANT>(a, grid, s);
     default: *why = "unknown epilogue"; return cudaErrorInvalidValue;
   }
 }

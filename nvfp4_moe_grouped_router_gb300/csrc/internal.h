@@ -17,12 +17,12 @@ struct QuantArgs {
   int64_t ldx;              // elements
   const int32_t* gather;    // nullable [rows]: output row p reads x row gather[p]
   const int32_t* offsets;   // nullable [G+1]: row groups (per-group global scale, grouped layout)
-  const int32_t* tile_offs; // [G+1], grouped layout only
+  const int32_t* tile_offs; // [G+1], TILED_GROUPED only
   int32_t G;
   const float* gs;          // [G] when offsets given, else [1]
-  uint8_t* codes;           // [rows, K/2]
-  uint8_t* scales;          // per layout
-  int layout;
+  uint8_t* codes;           // ROWMAJOR: [rows, K/2]; tiled layouts: the chunk buffer
+  uint8_t* scales;          // ROWMAJOR: [rows, K/16]; unused otherwise
+  int layout;               // OperandLayout
 };
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_global_scale(const void* x, int x_dtype, int64_t groups, int64_t n_per_group, float* gs_out,
@@ -44,6 +44,7 @@ struct RouteArgs {
 };
 int route_tokens_per_chunk(int32_t T);
 int route_num_chunks(int32_t T);
+int route_kernel_launches(int32_t T, int32_t k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
@@ -52,11 +53,9 @@ cudaError_t launch_combine(const float* y, int32_t H, const float* weights, cons
 enum GemmEpilogue : int { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_SWIGLU_QUANT = 2 };
 
 struct GemmArgs {
-  const uint8_t* a;         // [a_rows, K/2] codes
-  int64_t a_rows;           // capacity of a (rows the TMA may touch)
-  const uint8_t* a_sf;      // grouped-tile layout
-  const uint8_t* b;         // [G, N, K/2]
-  const uint8_t* b_sf;      // MMA layout, N rows per group
+  const uint8_t* a;         // TILED_GROUPED operand (K columns)
+  int64_t a_rows;           // rows the groups may hold (grid sizing)
+  const uint8_t* b;         // TILED operand of the [G*N, K] weights
   const float* gs_a;        // [G]
   const float* gs_b;        // [G]
   const int32_t* offsets;   // [G+1]
@@ -65,8 +64,7 @@ struct GemmArgs {
   int epilogue;
   void* d;                  // STORE: [rows, ldd]
   int64_t ldd;
-  uint8_t* q_codes;         // SWIGLU: [a_rows, N/4]
-  uint8_t* q_sf;            // SWIGLU: grouped-tile layout with K2 = N/2
+  uint8_t* q_codes;         // SWIGLU: TILED_GROUPED operand with K2 = N/2 (the next GEMM's A)
   const float* gs_q;        // SWIGLU: [G]
   float* h_dump;            // SWIGLU: nullable [a_rows, N/2]
   int* err;                 // device error word

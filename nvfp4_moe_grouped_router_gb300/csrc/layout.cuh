@@ -1,36 +1,59 @@
-// Scale-factor layouts shared by the quantizer, the GEMM epilogue and the GEMM
-// producer.  All three must agree byte for byte.
+// Operand layouts shared by the quantizer, the GEMM epilogue (which writes the
+// next GEMM's operand) and the GEMM producer.  All three must agree byte for
+// byte.
 //
-// The block-scaled FP4 MMA reads its scale factors from TMEM in 128-row x
-// 4-scale "atoms" (one atom per 128 rows per 64-element MMA K step).  An atom
-// is 512 contiguous bytes: row r, K-block b (0..3) lives at
-//     (r % 32) * 16 + (r / 32) * 4 + b
-// so that one tcgen05.cp 32x128b.warpx4 moves the whole atom to TMEM.
+// ROWMAJOR: codes [rows][K/2] (element 2j in the low nibble of byte j),
+//           scales [rows][K/16].
 //
-//   ROWMAJOR : scales[row][K/16]
-//   MMA      : atom (row / 128, k64) at ((row / 128) * (K / 64) + k64) * 512
-//   GROUPED  : rows grouped by offsets[G+1]; group g's rows are cut into
-//              128-row tiles numbered from tile_offsets[g] (the exclusive
-//              prefix of ceil(m_g / 128)); atom (tile, k64) at
-//              (tile * (K / 64) + k64) * 512.  Rows past a group's end in its
-//              last tile are never written.
+// TILED / TILED_GROUPED (what the GEMM consumes).  The GEMM streams both
+// operands with plain 1-D bulk copies, so operands are stored the way one
+// pipeline stage wants them in shared memory.  A matrix [rows, K] is cut into
+// 128-row tiles and 256-element K tiles; chunk (tile, kt) is TILE_BYTES
+// contiguous bytes:
+//   [0, 16384)      codes of rows 0..127, 128 bytes per row, with the 128-byte
+//                   swizzle already applied: code byte b of row r sits at
+//                   r * 128 + (((b / 16) ^ (r % 8)) * 16) + b % 16
+//   [16384, 18432)  four 512-byte scale atoms; atom kk covers K elements
+//                   64*kk .. 64*kk+63 of the K tile, and row r's 4 scales
+//                   (16 elements each) sit at (r % 32) * 16 + (r / 32) * 4 + b.
+//                   One tcgen05.cp 32x128b.warpx4 moves an atom into TMEM.
+// Chunks are ordered tile-major: chunk (tile, kt) at (tile * nkt + kt) *
+// TILE_BYTES with nkt = ceil(K / 256).  The first 8*j rows of a chunk are its
+// first 1024*j bytes, so a partial tile can be loaded by a prefix copy.
+// Bytes of rows past a group's end, and of K past K in the last K tile, are
+// never written and never used.
+//   TILED         : tile = row / 128 (weights: expert g's N rows are tiles
+//                   g*N/128 .. g*N/128 + N/128 - 1)
+//   TILED_GROUPED : rows grouped by offsets[G+1]; group g's rows form 128-row
+//                   tiles numbered from tile_offsets[g] (the exclusive prefix
+//                   of ceil(m_g / 128)): tile = tile_offsets[g] + (row - offsets[g]) / 128.
 #pragma once
 #include <cstdint>
 
 namespace nvf {
 
-enum SfLayout : int { SF_ROWMAJOR = 0, SF_MMA = 1, SF_GROUPED = 2 };
+enum OperandLayout : int { LAYOUT_ROWMAJOR = 0, LAYOUT_TILED = 1, LAYOUT_TILED_GROUPED = 2 };
+
+constexpr int TILE_ROWS = 128;
+constexpr int KT_ELEMS = 256;
+constexpr int TILE_CODE_BYTES = TILE_ROWS * KT_ELEMS / 2;   // 16384
+constexpr int TILE_SF_BYTES = 4 * 512;                      // 2048
+constexpr int TILE_BYTES = TILE_CODE_BYTES + TILE_SF_BYTES;  // 18432
 
 __host__ __device__ __forceinline__ uint32_t sf_atom_offset(uint32_t r128, uint32_t b4) {
   return (r128 & 31u) * 16u + (r128 >> 5) * 4u + b4;
 }
+__host__ __device__ __forceinline__ uint32_t tiled_code_offset(uint32_t r, uint32_t b) {
+  return r * 128u + ((((b >> 4) ^ (r & 7u)) << 4) | (b & 15u));
+}
+__host__ __device__ __forceinline__ int num_k_tiles(int K) { return (K + KT_ELEMS - 1) / KT_ELEMS; }
 
 // Largest g in [0, G) with offs[g] <= v (offs non-decreasing, offs[0] <= v < offs[G]).
-__device__ __forceinline__ int upper_group(const int32_t* __restrict__ offs, int G, int64_t v) {
+__device__ __forceinline__ int upper_group(const int32_t* offs, int G, int64_t v) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
-    if (static_cast<int64_t>(__ldg(offs + mid)) <= v) lo = mid; else hi = mid;
+    if (static_cast<int64_t>(offs[mid]) <= v) lo = mid; else hi = mid;
   }
   return lo;
 }

@@ -1,13 +1,11 @@
 // NVFP4 quantization kernels: per-tensor global scale (FP32 amax / 2688) and
 // the row quantizer, optionally gathering rows (the permute of tokens by
-// expert) and writing scales in the layout the block-scaled MMA reads.
+// expert) and writing the operand layouts the GEMM consumes.
 //
 // Method: FP4 E2M1 values with one unsigned E4M3 scale per 16 elements
 // (unsloth "Report: NVFP4 kernel selection on SM120/SM121", SASS paragraph
 // under "Why it matters": E2M1.E2M1.UE4M3.4X) and an FP32 block amax
 // (FlashInfer issue #2723, "What We Tried", item 2 "FP32 Amax Computation").
-// Each 16-element block: amax -> sb = E4M3(amax / (6 gs)) -> r = 1/(dec(sb) gs)
-// -> q = E2M1(x r), every step one correctly rounded FP32 operation.
 #include "internal.h"
 #include "layout.cuh"
 #include "ptx.cuh"
@@ -17,6 +15,8 @@
 
 namespace nvf {
 namespace {
+
+constexpr int kMaxSmemGroups = 4096;
 
 __device__ __forceinline__ void load64(const void* x, int xdt, int64_t off, float (&v)[64]) {
   if (xdt == X_BF16) {
@@ -41,37 +41,47 @@ __device__ __forceinline__ void load64(const void* x, int xdt, int64_t off, floa
   }
 }
 
+// One thread per (output row, 64-element group).  Group offsets (when given)
+// are staged in shared memory for the row -> group search.
 __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
-  const int gpr = a.K >> 6;  // 64-element groups per row: one per thread
+  extern __shared__ int32_t s_offs[];  // [G+1] offsets, [G+1] tile offsets
+  const bool grouped = a.offsets != nullptr;
+  const bool smem_offs = grouped && a.G < kMaxSmemGroups;
+  const int32_t* offs = a.offsets;
+  const int32_t* toffs = a.tile_offs;
+  if (smem_offs) {
+    for (int i = threadIdx.x; i <= a.G; i += blockDim.x) {
+      s_offs[i] = a.offsets[i];
+      s_offs[a.G + 1 + i] = a.tile_offs ? a.tile_offs[i] : 0;
+    }
+    __syncthreads();
+    offs = s_offs;
+    toffs = s_offs + a.G + 1;
+  }
+  const int gpr = a.K >> 6;  // 64-element groups per row
   const int64_t total = a.rows * gpr;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t p = idx / gpr;
     const int gg = static_cast<int>(idx - p * gpr);
     const int64_t src = a.gather ? static_cast<int64_t>(__ldg(a.gather + p)) : p;
-    const int g = a.offsets ? upper_group(a.offsets, a.G, p) : 0;
+    const int g = grouped ? upper_group(offs, a.G, p) : 0;
     const float gs = __ldg(a.gs + g);
-    const float six_gs = __fmul_rn(6.0f, gs);
     float v[64];
     load64(a.x, a.x_dtype, src * a.ldx + gg * 64, v);
     uint32_t w[8];
-    uint32_t sf = 0;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) sf |= quant_block16(v + 16 * b, gs, six_gs, w[2 * b], w[2 * b + 1]) << (8 * b);
-    uint4* dst = reinterpret_cast<uint4*>(a.codes + p * (a.K / 2) + gg * 32);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    size_t off;
-    if (a.layout == SF_ROWMAJOR) {
-      off = static_cast<size_t>(p) * (a.K / 16) + gg * 4;
-    } else if (a.layout == SF_MMA) {
-      off = (static_cast<size_t>(p >> 7) * gpr + gg) * 512 + sf_atom_offset(static_cast<uint32_t>(p & 127), 0);
-    } else {
-      const int64_t local = p - __ldg(a.offsets + g);
-      const int64_t tile = __ldg(a.tile_offs + g) + (local >> 7);
-      off = (static_cast<size_t>(tile) * gpr + gg) * 512 + sf_atom_offset(static_cast<uint32_t>(local & 127), 0);
+    const uint32_t sf = quant_group64(v, gs, w);
+    int64_t tile = 0;
+    uint32_t r = 0;
+    if (a.layout == LAYOUT_TILED) {
+      tile = p >> 7;
+      r = static_cast<uint32_t>(p & 127);
+    } else if (a.layout == LAYOUT_TILED_GROUPED) {
+      const int64_t local = p - offs[g];
+      tile = toffs[g] + (local >> 7);
+      r = static_cast<uint32_t>(local & 127);
     }
-    *reinterpret_cast<uint32_t*>(a.scales + off) = sf;
+    store_group64(a.codes, a.scales, a.layout, a.K, p, tile, r, gg, w, sf);
   }
 }
 
@@ -104,7 +114,8 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s) {
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
-  quantize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  const size_t smem = (a.offsets && a.G < kMaxSmemGroups) ? 2 * (a.G + 1) * sizeof(int32_t) : 0;
+  quantize_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,9 +1,12 @@
-// One 16-element NVFP4 block, shared by the row quantizer and the GEMM1
-// epilogue (which requantizes h = silu(gate) * up): FP32 amax, E4M3 block
-// scale of amax / (6 gs), reciprocal of dec(scale) * gs, E2M1 codes of x * r.
-// Every step is a single correctly rounded FP32 operation or a documented
-// round-to-nearest-even satfinite conversion instruction.
+// NVFP4 quantization of 16-element blocks, shared by the row quantizer, the
+// fused route+quantize kernel and the GEMM1 epilogue (which requantizes
+// h = silu(gate) * up): FP32 amax, E4M3 block scale of amax / (6 gs),
+// reciprocal of dec(scale) * gs, E2M1 codes of x * r.  Every step is a single
+// correctly rounded FP32 operation or a round-to-nearest-even satfinite
+// conversion instruction.  Also the stores of 64-element groups into each
+// operand layout.
 #pragma once
+#include "layout.cuh"
 #include "ptx.cuh"
 
 namespace nvf {
@@ -24,6 +27,35 @@ __device__ __forceinline__ uint32_t quant_block16(const float* v, float gs, floa
   w0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
   w1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
   return sb;
+}
+
+// 64 values -> 32 code bytes (w[0..7]) and 4 scale bytes (returned, block b in byte b).
+__device__ __forceinline__ uint32_t quant_group64(const float (&v)[64], float gs, uint32_t (&w)[8]) {
+  const float six_gs = __fmul_rn(6.0f, gs);
+  uint32_t sf = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) sf |= quant_block16(v + 16 * b, gs, six_gs, w[2 * b], w[2 * b + 1]) << (8 * b);
+  return sf;
+}
+
+// Store one quantized 64-element group (K elements 64*gg .. 64*gg+63) of row p.
+//   ROWMAJOR: codes/scales row-major.
+//   TILED*:   `tile` and `r` locate the row's 128-row tile; codes holds the chunks.
+__device__ __forceinline__ void store_group64(uint8_t* codes, uint8_t* scales, int layout, int K, int64_t p,
+                                              int64_t tile, uint32_t r, int gg, const uint32_t (&w)[8],
+                                              uint32_t sf) {
+  if (layout == LAYOUT_ROWMAJOR) {
+    uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + gg * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint32_t*>(scales + p * (K / 16) + gg * 4) = sf;
+  } else {
+    uint8_t* chunk = codes + (static_cast<size_t>(tile) * num_k_tiles(K) + (gg >> 2)) * TILE_BYTES;
+    const uint32_t b = static_cast<uint32_t>(gg & 3) * 32u;
+    *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, b)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, b + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint32_t*>(chunk + TILE_CODE_BYTES + (gg & 3) * 512 + sf_atom_offset(r, 0)) = sf;
+  }
 }
 
 }  // namespace nvf

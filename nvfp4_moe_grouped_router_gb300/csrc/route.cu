@@ -37,69 +37,79 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Top-k of one token by one warp.  NV = logits held per lane (E <= 32 * NV).
+// Writes ids / weights of token t and returns, in lanes j < k, the j-th
+// selected expert (-1 in the other lanes).
+template <int NV>
+__device__ __forceinline__ int topk_token(const RouteArgs& a, int t, int lane) {
+  const int E = a.E, k = a.k;
+  const float* row = a.logits + static_cast<int64_t>(t) * E;
+  float v[NV];
+  uint32_t taken = 0;  // bit i: value i of this lane is used or absent
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = i * 32 + lane;
+    if (e < E) {
+      v[i] = a.bias ? __fadd_rn(__ldg(row + e), __ldg(a.bias + e)) : __ldg(row + e);
+    } else {
+      v[i] = 0.0f;
+      taken |= 1u << i;
+    }
+  }
+  float sel_v = 0.0f;
+  int sel_e = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      // indices grow with i, so a strict '>' keeps the lower id on ties
+      if (!((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
+        bv = v[i];
+        bi = i * 32 + lane;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const bool better = (oi != 0x7fffffff) && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+      if (better) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) { sel_v = bv; sel_e = bi; }
+  }
+  const float m = __shfl_sync(0xffffffffu, sel_v, 0);
+  const float p = (lane < k) ? expf(sel_v - m) : 0.0f;
+  float denom;
+  if (a.renormalize) {
+    denom = warp_sum(p);
+  } else {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (i * 32 + lane < E) s += expf(v[i] - m);
+    denom = warp_sum(s);
+  }
+  if (lane < k) {
+    a.ids[static_cast<int64_t>(t) * k + lane] = sel_e;
+    a.weights[static_cast<int64_t>(t) * k + lane] = p / denom;
+  }
+  return sel_e;
+}
+
+template <int NV>
 __global__ void __launch_bounds__(kTopkWarps * 32) route_topk_kernel(RouteArgs a, int tpc) {
   extern __shared__ int hist[];  // [E]
-  const int E = a.E, k = a.k;
+  const int E = a.E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * tpc;
   const int t1 = min(a.T, t0 + tpc);
   for (int t = t0 + warp; t < t1; t += kTopkWarps) {
-    const float* row = a.logits + static_cast<int64_t>(t) * E;
-    float v[kPerLane];
-    uint32_t taken = 0;  // bit i: value i of this lane is used or absent
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E) {
-        const float b = a.bias ? __ldg(a.bias + e) : 0.0f;
-        v[i] = a.bias ? __fadd_rn(__ldg(row + e), b) : __ldg(row + e);
-      } else {
-        v[i] = 0.0f;
-        taken |= 1u << i;
-      }
-    }
-    float sel_v = 0.0f;
-    int sel_e = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = 0.0f;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i) {
-        // indices grow with i, so a strict '>' keeps the lower id on ties
-        if (!((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
-          bv = v[i];
-          bi = i * 32 + lane;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const bool better = (oi != 0x7fffffff) && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-        if (better) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) { sel_v = bv; sel_e = bi; }
-    }
-    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
-    const float p = (lane < k) ? expf(sel_v - m) : 0.0f;
-    float denom;
-    if (a.renormalize) {
-      denom = warp_sum(p);
-    } else {
-      float s = 0.0f;
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i)
-        if (i * 32 + lane < E) s += expf(v[i] - m);
-      denom = warp_sum(s);
-    }
-    if (lane < k) {
-      a.ids[static_cast<int64_t>(t) * k + lane] = sel_e;
-      a.weights[static_cast<int64_t>(t) * k + lane] = p / denom;
-      atomicAdd(&hist[sel_e], 1);
-    }
+    const int e = topk_token<NV>(a, t, lane);
+    if (e >= 0) atomicAdd(&hist[e], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
@@ -249,13 +259,100 @@ int route_num_chunks(int32_t T) {
   return T == 0 ? 0 : (T + tpc - 1) / tpc;
 }
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+namespace {
+
+constexpr int kSmallAssign = 4096;   // T*k handled by the single-CTA path
+
+// Small batches: top-k, histogram, prefix sums and the stable scatter in one
+// CTA of 32 warps: one launch, no scratch memory.
+template <int NV>
+__global__ void __launch_bounds__(1024) route_small_kernel(RouteArgs a) {
+  __shared__ int cnt[kMaxE + 1];
+  __shared__ int til[kMaxE + 1];
+  __shared__ int s_ids[kSmallAssign];
+  const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) cnt[e] = (e < E) ? 0 : T;  // shared expert: every token
+  __syncthreads();
+  for (int t = warp; t < T; t += 32) {
+    const int e = topk_token<NV>(a, t, lane);
+    if (e >= 0) {
+      s_ids[t * k + lane] = e;
+      atomicAdd(&cnt[e], 1);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int e = lane; e < Et; e += 32) til[e] = (cnt[e] + 127) >> 7;
+    __syncwarp();
+    const int tot = warp_exclusive_scan(cnt, Et, lane);
+    const int ttot = warp_exclusive_scan(til, Et, lane);
+    __syncwarp();
+    for (int e = lane; e < Et; e += 32) {
+      a.offsets[e] = cnt[e];
+      a.tile_offs[e] = til[e];
+    }
+    if (lane == 0) {
+      a.offsets[Et] = tot;
+      a.tile_offs[Et] = ttot;
+    }
+    // Stable scatter in assignment order; cnt[e] is now expert e's next free slot.
+    const int R = T * k;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = 0; base < R; base += 32) {
+      const int as = base + lane;
+      const bool active = as < R;
+      const uint32_t mask = __ballot_sync(0xffffffffu, active);
+      int e = 0;
+      uint32_t peers = 0;
+      if (active) {
+        e = s_ids[as];
+        peers = __match_any_sync(mask, e);
+        const int pos = cnt[e] + __popc(peers & lt);
+        a.perm_to_src[pos] = as;
+        a.src_to_perm[as] = pos;
+        a.perm_token[pos] = as / k;
+      }
+      __syncwarp();
+      if (active && lane == 31 - __clz(peers)) cnt[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  if (a.shared) {
+    const int R = T * k;
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      a.perm_to_src[R + t] = R + t;
+      a.src_to_perm[R + t] = R + t;
+      a.perm_token[R + t] = t;
+    }
+  }
+}
+
+template <int NV>
+cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
+  if (static_cast<int64_t>(a.T) * a.k <= kSmallAssign) {
+    route_small_kernel<NV><<<1, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   const int tpc = route_tokens_per_chunk(a.T);
   const int nch = route_num_chunks(a.T);
-  if (nch > 0) route_topk_kernel<<<nch, kTopkWarps * 32, a.E * sizeof(int), s>>>(a, tpc);
+  route_topk_kernel<NV><<<nch, kTopkWarps * 32, a.E * sizeof(int), s>>>(a, tpc);
   route_scan_kernel<<<1, 1024, 0, s>>>(a, nch);
-  if (nch > 0) route_scatter_kernel<<<nch, 32, a.E * sizeof(int), s>>>(a, tpc);
+  route_scatter_kernel<<<nch, 32, a.E * sizeof(int), s>>>(a, tpc);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int route_kernel_launches(int32_t T, int32_t k) {
+  return static_cast<int64_t>(T) * k <= kSmallAssign ? 1 : 3;
+}
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+  if (a.E <= 128) return launch_route_nv<4>(a, s);
+  if (a.E <= 256) return launch_route_nv<8>(a, s);
+  if (a.E <= 512) return launch_route_nv<16>(a, s);
+  return launch_route_nv<32>(a, s);
 }
 
 cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,

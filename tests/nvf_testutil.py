@@ -19,61 +19,53 @@ def ensure_built():
     return build.build()
 
 
+TILE_BYTES = 18432
+TILE_CODE_BYTES = 16384
+
+
 def atom_index(r128, b4):
     return (r128 % 32) * 16 + (r128 // 32) * 4 + b4
 
 
-def unswizzle_mma(sf: np.ndarray, rows: int, K: int) -> np.ndarray:
-    """NVF_SF_MMA bytes -> [rows, K/16]."""
-    sf = np.asarray(sf, dtype=np.uint8).reshape(-1)
-    r = np.arange(rows)[:, None]
-    kb = np.arange(K // 16)[None, :]
-    off = ((r // 128) * (K // 64) + kb // 4) * 512 + atom_index(r % 128, kb % 4)
-    return sf[off]
-
-
-def unswizzle_grouped(sf: np.ndarray, offsets, tile_offsets, K: int) -> np.ndarray:
-    """NVF_SF_GROUPED bytes -> [offsets[-1], K/16] for the rows of every group."""
-    sf = np.asarray(sf, dtype=np.uint8).reshape(-1)
+def row_tiles(rows: int, offsets=None, tile_offsets=None):
+    """(tile, r) of every row: TILED when offsets is None, else TILED_GROUPED."""
+    p = np.arange(rows)
+    if offsets is None:
+        return p // 128, p % 128
     offsets = np.asarray(offsets, dtype=np.int64)
     tile_offsets = np.asarray(tile_offsets, dtype=np.int64)
-    R = int(offsets[-1])
-    out = np.zeros((R, K // 16), np.uint8)
+    g = np.searchsorted(offsets, p, side="right") - 1
+    local = p - offsets[g]
+    return tile_offsets[g] + local // 128, local % 128
+
+
+def _tiled_index(tile, r, K):
+    """Byte offsets of every code byte [rows, K/2] and scale byte [rows, K/16]."""
+    nkt = (K + 255) // 256
+    tile = np.asarray(tile, dtype=np.int64)[:, None]
+    r = np.asarray(r, dtype=np.int64)[:, None]
+    b = np.arange(K // 2)[None, :]
+    kt, bb = b // 128, b % 128
+    code = (tile * nkt + kt) * TILE_BYTES + r * 128 + (((bb // 16) ^ (r % 8)) * 16) + bb % 16
     kb = np.arange(K // 16)[None, :]
-    for g in range(len(offsets) - 1):
-        lo, hi = offsets[g], offsets[g + 1]
-        if hi == lo:
-            continue
-        local = np.arange(hi - lo)[:, None]
-        tile = tile_offsets[g] + local // 128
-        off = (tile * (K // 64) + kb // 4) * 512 + atom_index(local % 128, kb % 4)
-        out[lo:hi] = sf[off]
-    return out
+    kt2, kk, s = kb // 16, (kb % 16) // 4, kb % 4
+    sf = (tile * nkt + kt2) * TILE_BYTES + TILE_CODE_BYTES + kk * 512 + atom_index(r % 128, s)
+    return code, sf
 
 
-def grouped_from_rowmajor(scales: np.ndarray, offsets, tile_offsets, K: int, nbytes: int) -> np.ndarray:
-    """[R, K/16] -> NVF_SF_GROUPED bytes (inverse of unswizzle_grouped; other bytes 0)."""
+def tiled_unpack(buf, K, tile, r):
+    """Tiled operand bytes -> (codes [rows, K/2], scales [rows, K/16]) for rows at (tile, r)."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    code, sf = _tiled_index(tile, r, K)
+    return buf[code], buf[sf]
+
+
+def tiled_pack(codes, scales, K, tile, r, nbytes):
+    """Inverse of tiled_unpack; bytes not covered stay 0."""
     out = np.zeros(nbytes, np.uint8)
-    offsets = np.asarray(offsets, dtype=np.int64)
-    tile_offsets = np.asarray(tile_offsets, dtype=np.int64)
-    kb = np.arange(K // 16)[None, :]
-    for g in range(len(offsets) - 1):
-        lo, hi = offsets[g], offsets[g + 1]
-        if hi == lo:
-            continue
-        local = np.arange(hi - lo)[:, None]
-        tile = tile_offsets[g] + local // 128
-        off = (tile * (K // 64) + kb // 4) * 512 + atom_index(local % 128, kb % 4)
-        out[off] = scales[lo:hi]
-    return out
-
-
-def mma_from_rowmajor(scales: np.ndarray, rows: int, K: int) -> np.ndarray:
-    out = np.zeros((rows + 127) // 128 * 128 * (K // 16), np.uint8)
-    r = np.arange(rows)[:, None]
-    kb = np.arange(K // 16)[None, :]
-    off = ((r // 128) * (K // 64) + kb // 4) * 512 + atom_index(r % 128, kb % 4)
-    out[off] = scales
+    code, sf = _tiled_index(tile, r, K)
+    out[code] = codes
+    out[sf] = scales
     return out
 
 

@@ -50,14 +50,15 @@ def test_host_helpers(nvf):
     assert sorted(nvf.w13_row_map(192)) == list(range(384))
     with pytest.raises(nvf.NvfError):
         nvf.w13_row_map(100)
-    assert nvf.grouped_scale_bytes(300, 4, 256) == (3 + 4) * 128 * 16
+    assert nvf.tiled_bytes(300, 4, 256) == (3 + 4) * 1 * 18432
+    assert nvf.tiled_bytes(256, 0, 768) == 2 * 3 * 18432
 
 
 def test_workspace_layout(nvf):
     L = nvf.workspace_layout(256, 512, 4096, 1024, 10, True)
     assert L["R"] == 256 * 11
     offs = [L[n] for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src", "src_to_perm",
-                           "perm_token", "route_scratch", "a1_codes", "a1_sf", "a2_codes", "a2_sf", "y")]
+                           "perm_token", "route_scratch", "a1", "a2", "y")]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and L["total"] > offs[-1] + L["R"] * 4096 * 4 - 256
     with pytest.raises(nvf.NvfError):

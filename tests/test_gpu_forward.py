@@ -23,8 +23,8 @@ from oracle import formats as F
 from oracle import moe as M
 from synth import CONFIGS, expert_weights, make_inputs
 from tests import oracle_pool
-from tests.nvf_testutil import (ROOT, dequant_check, ensure_built, quantize_rows_check, rel_err, unswizzle_grouped,
-                                 unswizzle_mma, w13_prepared_rows)
+from tests.nvf_testutil import (ROOT, dequant_check, ensure_built, quantize_rows_check, rel_err, row_tiles,
+                                 tiled_unpack, w13_prepared_rows)
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -114,24 +114,23 @@ def check_layer(nvf, layer, out_dtype=torch.float32, tokens=None):
     rows = np.zeros(R, bool)
     for e in experts:
         rows[offs[e]:offs[e + 1]] = True
-    a1c = ws[L["a1_codes"]:L["a1_codes"] + R * cfg.H // 2].cpu().numpy().reshape(R, cfg.H // 2)
-    a1s = unswizzle_grouped(ws[L["a1_sf"]:].cpu().numpy(), offs, tiles, cfg.H)
-    a2c = ws[L["a2_codes"]:L["a2_codes"] + R * cfg.I // 2].cpu().numpy().reshape(R, cfg.I // 2)
-    a2s = unswizzle_grouped(ws[L["a2_sf"]:].cpu().numpy(), offs, tiles, cfg.I)
+    wsn = ws.cpu().numpy()
+    tr = row_tiles(R, offs, tiles)
+    a1c, a1s = tiled_unpack(wsn[L["a1"]:L["a2"]], cfg.H, *tr)
+    a2c, a2s = tiled_unpack(wsn[L["a2"]:L["y"]], cfg.I, *tr)
     y = _ws_view(ws, L, "y", R * cfg.H, np.float32).reshape(R, cfg.H)
     h = h_gpu.cpu().numpy()
     assert np.array_equal(a1c[rows], ref["a1_codes"][rows])
     assert np.array_equal(a1s[rows], ref["a1_scales"][rows])
     # prepared weights equal the oracle's quantization (w13 rows reordered)
     perm = w13_prepared_rows(cfg.I)
-    n13, n2 = 2 * cfg.I * cfg.H // 16, cfg.H * cfg.I // 16
+    n13, n2 = nvf.tiled_bytes(2 * cfg.I, 0, cfg.H), nvf.tiled_bytes(cfg.H, 0, cfg.I)
     for e in experts[:3] + experts[-2:]:
         c13, s13, g13, c2, s2, g2 = layer.ocache[e]
-        assert np.array_equal(layer.wts.w13[e].cpu().numpy(), c13[perm])
-        assert np.array_equal(unswizzle_mma(layer.wts.w13_sf[e * n13:(e + 1) * n13].cpu().numpy(), 2 * cfg.I, cfg.H),
-                              s13[perm])
-        assert np.array_equal(layer.wts.w2[e].cpu().numpy(), c2)
-        assert np.array_equal(unswizzle_mma(layer.wts.w2_sf[e * n2:(e + 1) * n2].cpu().numpy(), cfg.H, cfg.I), s2)
+        gc13, gs13 = tiled_unpack(layer.wts.w13[e * n13:(e + 1) * n13].cpu().numpy(), cfg.H, *row_tiles(2 * cfg.I))
+        assert np.array_equal(gc13, c13[perm]) and np.array_equal(gs13, s13[perm])
+        gc2, gs2 = tiled_unpack(layer.wts.w2[e * n2:(e + 1) * n2].cpu().numpy(), cfg.I, *row_tiles(cfg.H))
+        assert np.array_equal(gc2, c2) and np.array_equal(gs2, s2)
         assert layer.wts.gs_w13[e].item() == g13 and layer.wts.gs_w2[e].item() == g2
     assert rel_err(h[rows], ref["h"][rows]) <= TOL
     # A2 is a valid requantization of the GPU's own h (independent checker, bit-exact)

@@ -11,7 +11,7 @@ import torch
 
 from oracle import formats as F
 from oracle import moe as M
-from tests.nvf_testutil import ensure_built, grouped_from_rowmajor, mma_from_rowmajor, rel_err
+from tests.nvf_testutil import ensure_built, rel_err, row_tiles, tiled_pack
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -35,16 +35,15 @@ def _run(nvf, a_codes, a_scales, sizes, w_codes, w_scales, gs_a, gs_w, out_dtype
     offs = np.concatenate([[0], np.cumsum(sizes)])
     tiles = M.tile_offsets(sizes)
     R = int(offs[-1])
-    rows = R + pad_rows
-    A = np.zeros((max(rows, 1), Kh), np.uint8)
-    A[:R] = a_codes
-    nbytes = nvf.grouped_scale_bytes(max(rows, 1), G, K)
-    a_sf = grouped_from_rowmajor(a_scales, offs, tiles, K, nbytes)
-    b_sf = mma_from_rowmajor(w_scales.reshape(G * N, K // 16), G * N, K)
-    dev = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    D = nvf.grouped_gemm(dev(A), dev(a_sf), dev(w_codes), dev(b_sf), dev(np.asarray(gs_a, np.float32)),
-                         dev(np.asarray(gs_w, np.float32)), dev(offs.astype(np.int32)), dev(tiles.astype(np.int32)),
-                         N, K, out_dtype)
+    rows = max(R + pad_rows, 1)
+    ta, ra = row_tiles(R, offs, tiles)
+    A = tiled_pack(a_codes, a_scales, K, ta, ra, nvf.tiled_bytes(rows, G, K))
+    tb, rb = row_tiles(G * N)
+    B = tiled_pack(w_codes.reshape(G * N, Kh), w_scales.reshape(G * N, K // 16), K, tb, rb,
+                   nvf.tiled_bytes(G * N, 0, K))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    D = nvf.grouped_gemm(dev(A), rows, dev(B), dev(np.asarray(gs_a, np.float32)), dev(np.asarray(gs_w, np.float32)),
+                         dev(offs.astype(np.int32)), dev(tiles.astype(np.int32)), N, K, out_dtype)
     code, detail = nvf.device_status()
     assert code == 0, f"device error word {code} at {detail}"
     return D.float().cpu().numpy()[:R], offs
@@ -121,10 +120,10 @@ def test_random_within_tolerance(nvf, sizes, N, K, out_dtype):
 
 
 def test_argument_validation(nvf):
-    z = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     f = torch.ones(1, dtype=torch.float32, device="cuda")
     o = torch.tensor([0, 0], dtype=torch.int32, device="cuda")
     with pytest.raises(nvf.NvfError, match="N=100"):
-        nvf.grouped_gemm(z.view(2, 128), z, z.view(1, 2, 128), z, f, f, o, o, 100, 256)
+        nvf.grouped_gemm(z, 2, z, f, f, o, o, 100, 256)
     with pytest.raises(nvf.NvfError, match="K=100"):
-        nvf.grouped_gemm(z.view(4, 64), z, z.view(1, 2, 128), z, f, f, o, o, 128, 100)
+        nvf.grouped_gemm(z, 2, z, f, f, o, o, 128, 100)

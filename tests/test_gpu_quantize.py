@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from oracle import formats as F
-from tests.nvf_testutil import ensure_built, unswizzle_grouped, unswizzle_mma
+from tests.nvf_testutil import ensure_built, row_tiles, tiled_unpack
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ def _gpu_quant(nvf, x, gs, layout=0, **kw):
     g = torch.tensor([gs], dtype=torch.float32, device="cuda") if np.isscalar(gs) else gs
     c, s = nvf.quantize(x, g, layout, **kw)
     torch.cuda.synchronize()
-    return c.cpu().numpy(), s.cpu().numpy()
+    return c.cpu().numpy(), (None if s is None else s.cpu().numpy())
 
 
 def _check_rowmajor(nvf, x, gs):
@@ -63,26 +63,28 @@ def test_ties_signed_zero_and_saturation(nvf):
 
 
 @pytest.mark.parametrize("layout", [1, 2])
-def test_scale_layouts(nvf, layout):
-    rows, K = 517, 512
+@pytest.mark.parametrize("K", [512, 320, 64])
+def test_tiled_layouts(nvf, layout, K):
+    rows = 517
     x = torch.randn(rows, K, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
     gs = F.global_scale(float(x.float().abs().max()))
     ref_c, ref_s = F.quantize_rows(x.float().numpy(), gs)
     if layout == 1:
-        c, s = _gpu_quant(nvf, x.cuda(), gs, layout=1)
-        assert np.array_equal(unswizzle_mma(s, rows, K), ref_s)
+        buf, _ = _gpu_quant(nvf, x.cuda(), gs, layout=1)
+        tile, r = row_tiles(rows)
     else:
         sizes = np.array([0, 130, 1, 0, 256, 127, 3], np.int64)
         sizes[-1] = rows - sizes[:-1].sum()
         offs = np.concatenate([[0], np.cumsum(sizes)])
         tiles = np.concatenate([[0], np.cumsum((sizes + 127) // 128)])
-        G = len(sizes)
-        gsv = torch.full((G,), float(gs), dtype=torch.float32, device="cuda")
-        c, s = _gpu_quant(nvf, x.cuda(), gsv, layout=2,
-                          offsets=torch.tensor(offs, dtype=torch.int32, device="cuda"),
-                          tile_offsets=torch.tensor(tiles, dtype=torch.int32, device="cuda"))
-        assert np.array_equal(unswizzle_grouped(s, offs, tiles, K), ref_s)
+        gsv = torch.full((len(sizes),), float(gs), dtype=torch.float32, device="cuda")
+        buf, _ = _gpu_quant(nvf, x.cuda(), gsv, layout=2,
+                            offsets=torch.tensor(offs, dtype=torch.int32, device="cuda"),
+                            tile_offsets=torch.tensor(tiles, dtype=torch.int32, device="cuda"))
+        tile, r = row_tiles(rows, offs, tiles)
+    c, s_ = tiled_unpack(buf, K, tile, r)
     assert np.array_equal(c, ref_c)
+    assert np.array_equal(s_, ref_s)
 
 
 def test_gather_and_per_group_scales(nvf):
