@@ -37,8 +37,16 @@ sys.path.insert(0, ROOT)
 from synth import CONFIGS, expert_weights, make_inputs  # noqa: E402
 
 METRIC = "NVFP4 MoE layer tokens/s; grouped-GEMM % FP4 TC peak (prefill) / % HBM (decode)"
-STAGES = ["route_permute", "quantize_a1", "gate_up_gemm_swiglu_quant", "down_gemm", "combine"]
-KERNELS_PER_STEP = 7   # route: topk, scan, scatter; quantize; two GEMMs; combine
+# (name, first event, last event) of the forward's six stage events; events 1 and 2
+# bracket the separate activation quantization, which the route kernel now does.
+STAGES = [("route_permute_quant_a1", 0, 1), ("gate_up_gemm_swiglu_quant", 2, 3), ("down_gemm", 3, 4),
+          ("combine", 4, 5)]
+
+
+def kernels_per_step(T):
+    """Kernels one forward launches: top-k, (prefix for > 256 tokens), permute+quantize,
+    gate_up GEMM, down GEMM, combine."""
+    return 1 + (1 if (T + 31) // 32 > 8 else 0) + 1 + 2 + 1
 
 
 def load_peaks():
@@ -240,13 +248,16 @@ def main():
         if code != 0:
             raise RuntimeError(f"device error word {code} at {detail}")
         print(json.dumps({"profile_run": cfg.name, "steps": args.steps, "warmup": max(3, args.warmup),
-                          "kernels_per_step": KERNELS_PER_STEP}))
+                          "kernels_per_step": kernels_per_step(cfg.T)}))
         return
 
-    # --- graph of the K timed steps, with per-stage events inside
+    # --- graph of the K timed steps (kernels chained by programmatic dependent
+    # launch), and a second graph with an event at every stage boundary for the
+    # per-stage breakdown (events serialise the kernels, so it is timed apart).
     K = args.steps
     chunk = min(K, 256)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(chunk)]
+    n_ev = 6
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(chunk)]
     for row in ev:          # torch creates the CUDA event on first record
         for e in row:
             e.record()
@@ -259,12 +270,17 @@ def main():
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    step(ev[i])
+                    step()
             graphs.append((n, g))
+        g_stages = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_stages, stream=stream):
+            for i in range(chunk):
+                step(ev[i])
     torch.cuda.current_stream().wait_stream(stream)
     plan = [graphs[0]] * (K // chunk) + ([g for g in graphs if g[0] == K % chunk] if K % chunk else [])
     for n, g in graphs:    # warm the graphs
         g.replay()
+    g_stages.replay()
     torch.cuda.synchronize()
 
     out_dir = os.path.join(ROOT, "gpurun_out")
@@ -299,10 +315,11 @@ def main():
     if code != 0:
         raise RuntimeError(f"device error word {code} at {detail}")
 
-    # per-stage durations of the last replayed chunk
-    last_n = plan[-1][0]
-    stage_ms = {s: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(last_n))
-                for j, s in enumerate(STAGES)}
+    # per-stage durations from the event graph
+    g_stages.replay()
+    torch.cuda.synchronize()
+    stage_ms = {s: statistics.mean(ev[i][a].elapsed_time(ev[i][b]) for i in range(chunk)) for s, a, b in STAGES}
+    stage_step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][5]) for i in range(chunk))
 
     # --- end to end through the C ABI with host buffers
     xh = x.cpu().pin_memory()
@@ -353,10 +370,12 @@ def main():
                                    f"{'+1 shared' if cfg.shared else ''} top-{cfg.k})",
                        "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "shared": cfg.shared,
                        "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (weights streamed per step)",
-                       "timing": "CUDA graph of the K steps, CUDA events"},
-            "stage_ms": stage_ms, "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
+                       "timing": "CUDA graph of the K steps (programmatic dependent launch between kernels), "
+                                 "CUDA events; stage_ms from a second graph with events at stage boundaries"},
+            "stage_ms": stage_ms, "stage_graph_ms_per_step": stage_step_ms,
+            "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
             "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
-            "roofline": roof, "clocks": clk, "gpu_launches": KERNELS_PER_STEP * K,
+            "roofline": roof, "clocks": clk, "gpu_launches": kernels_per_step(cfg.T) * K,
             "e2e": {"value": cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
                     "d2h_bytes_per_step": out.numel() * 4}}

@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 namespace nvf {
 
@@ -78,6 +80,16 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
 int sm_count() { return g_cur_sms; }
+
+void prefer_max_shared(const void* func) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.insert({dev, func}).second)
+    cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
 void set_last_error(const char* msg) {
   std::snprintf(g_msg, sizeof(g_msg), "%s", msg);
 }
@@ -107,6 +119,22 @@ using namespace nvf;
     cudaError_t e_ = (call);                       \
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
+
+namespace {
+RouteArgs make_route_args(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k, int32_t renormalize,
+                          int32_t shared, int32_t* ids, float* w, int32_t* offsets, int32_t* tile_offsets,
+                          int32_t* perm_to_src, int32_t* src_to_perm, int32_t* perm_token, void* scratch) {
+  RouteArgs a{};
+  a.logits = logits; a.bias = bias; a.T = T; a.E = E; a.k = k; a.renormalize = renormalize ? 1 : 0;
+  a.shared = shared; a.ids = ids; a.weights = w; a.offsets = offsets; a.tile_offs = tile_offsets;
+  a.perm_to_src = perm_to_src; a.src_to_perm = src_to_perm; a.perm_token = perm_token;
+  const size_t W = (static_cast<size_t>(T) + 31) / 32;
+  a.words = static_cast<uint32_t*>(scratch);
+  a.prefix = reinterpret_cast<int32_t*>(a.words + W * E);
+  a.counts = a.prefix + W * E;
+  return a;
+}
+}  // namespace
 
 extern "C" {
 
@@ -195,7 +223,7 @@ nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t 
 nvf_status moe_route_permute_workspace_size(int32_t T, int32_t E, size_t* bytes) {
   g_msg[0] = 0;
   NVF_REQUIRE(bytes != nullptr && T >= 0 && E >= 1, "bad arguments");
-  *bytes = align256(2 * static_cast<size_t>(route_num_chunks(T)) * E * sizeof(int32_t));
+  *bytes = align256(route_scratch_bytes(T, E));
   if (*bytes == 0) *bytes = 256;
   return NVF_OK;
 }
@@ -226,10 +254,8 @@ nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, 
   moe_route_permute_workspace_size(T, E, &need);
   NVF_REQUIRE(ws != nullptr || need == 0, "ws must not be NULL");
   if (ws_bytes < need) return fail(NVF_ERR_WORKSPACE, "workspace %zu bytes < %zu needed (T=%d E=%d)", ws_bytes, need, T, E);
-  const int nch = route_num_chunks(T);
-  RouteArgs a{logits, bias, T, E, k, renormalize ? 1 : 0, shared_expert, topk_ids, topk_w, expert_offsets,
-              tile_offsets, perm_to_src, src_to_perm, perm_token, static_cast<int32_t*>(ws),
-              static_cast<int32_t*>(ws) + static_cast<size_t>(nch) * E};
+  RouteArgs a = make_route_args(logits, bias, T, E, k, renormalize, shared_expert, topk_ids, topk_w, expert_offsets,
+                                tile_offsets, perm_to_src, src_to_perm, perm_token, ws);
   NVF_CUDA(launch_route(a, static_cast<cudaStream_t>(stream)), "route launch");
   return NVF_OK;
 }
@@ -335,7 +361,6 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   auto i32 = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
-  const int nch = route_num_chunks(T);
   auto mark = [&](int i) -> cudaError_t {
     // External records become event nodes when the stream is being captured into a graph.
     return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal)
@@ -343,16 +368,22 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   };
   NVF_CUDA(mark(0), "cudaEventRecord");
 
-  RouteArgs ra{logits, bias, T, E, k, renormalize ? 1 : 0, w->shared, i32(L.topk_ids),
-               reinterpret_cast<float*>(base + L.topk_w), i32(L.expert_offsets), i32(L.tile_offsets),
-               i32(L.perm_to_src), i32(L.src_to_perm), i32(L.perm_token), i32(L.route_scratch),
-               i32(L.route_scratch) + static_cast<size_t>(nch) * E};
+  // routing, permutation and the activation quantization (A1) in one pass
+  RouteArgs ra = make_route_args(logits, bias, T, E, k, renormalize, w->shared, i32(L.topk_ids),
+                                 reinterpret_cast<float*>(base + L.topk_w), i32(L.expert_offsets),
+                                 i32(L.tile_offsets), i32(L.perm_to_src), i32(L.src_to_perm), i32(L.perm_token),
+                                 base + L.route_scratch);
+  ra.x = x;
+  ra.H = H;
+  ra.gs_a1 = gs_a1;
+  ra.a1 = base + L.a1;
+  // Kernels after the first start while their predecessor drains (programmatic
+  // dependent launch), unless stage boundaries are being timed: an event
+  // between two kernels is a full dependency.
+  const bool pdl = stage_events == nullptr;
   NVF_CUDA(launch_route(ra, s), "route launch");
   NVF_CUDA(mark(1), "cudaEventRecord");
 
-  QuantArgs qa{x, NVF_BF16, L.R, H, H, i32(L.perm_token), i32(L.expert_offsets), i32(L.tile_offsets), Et,
-               gs_a1, base + L.a1, nullptr, NVF_LAYOUT_TILED_GROUPED};
-  NVF_CUDA(launch_quantize(qa, s), "activation quantize launch");
   NVF_CUDA(mark(2), "cudaEventRecord");
 
   const char* why = nullptr;
@@ -361,7 +392,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g1.b = w->w13; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
   g1.offsets = i32(L.expert_offsets); g1.tile_offs = i32(L.tile_offsets); g1.G = Et; g1.N = 2 * I; g1.K = H;
   g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2; g1.gs_q = gs_a2;
-  g1.h_dump = h_dump; g1.err = dev_->err;
+  g1.h_dump = h_dump; g1.err = dev_->err; g1.pdl = pdl;
   cudaError_t e = launch_grouped_gemm(g1, s, &why);
   if (e != cudaSuccess)
     return fail(NVF_ERR_CUDA, "gate_up GEMM (E'=%d R=%lld N=%d K=%d): %s", Et, (long long)L.R, 2 * I, H,
@@ -373,6 +404,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g2.b = w->w2; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
   g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
+  g2.pdl = pdl; g2.early_weights = pdl;  // expert offsets come from the route, two kernels back
   e = launch_grouped_gemm(g2, s, &why);
   if (e != cudaSuccess)
     return fail(NVF_ERR_CUDA, "down GEMM (E'=%d R=%lld N=%d K=%d): %s", Et, (long long)L.R, H, I,
@@ -380,7 +412,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   NVF_CUDA(mark(4), "cudaEventRecord");
 
   NVF_CUDA(launch_combine(reinterpret_cast<const float*>(base + L.y), H, reinterpret_cast<const float*>(base + L.topk_w),
-                          i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s),
+                          i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s, pdl),
            "combine launch");
   NVF_CUDA(mark(5), "cudaEventRecord");
   return NVF_OK;

@@ -8,24 +8,41 @@
 // "Purpose": nvfp4_blockwise_moe_kernel.cu) with a per-expert alpha and beta = 0
 // (vLLM PR #29242 review: alpha_ptr_array, beta = 0.0f).
 //
-// Design (one CTA per SM, persistent, 320 threads):
-//   warp 0    producer: per pipeline stage one contiguous 18 KB chunk of B
-//             (128 weight rows x 256 K, codes pre-swizzled + scale atoms) and
-//             the valid-row prefix of the matching A chunk, moved with 1-D
-//             bulk copies (cp.async.bulk) into a STAGES-deep ring guarded by
-//             mbarrier full/empty pairs.  Weights therefore stream from HBM as
-//             sequential 18 KB runs.
-//   warp 1    TMEM owner and MMA issuer: per stage, tcgen05.cp the scale atoms
-//             into TMEM, then four 128x128x64 block-scaled MMAs into one of two
-//             FP32 TMEM accumulators (128 columns each).
-//   warps 2-9 epilogue: two warps per 32-lane TMEM quarter, 64 columns each;
-//             tcgen05.ld, scale by alpha, then either store FP32/BF16 rows or
-//             compute h = silu(gate) * up and requantize it to NVFP4 straight
-//             into the next GEMM's tiled operand.  Warps whose 32 rows are all
-//             past the group's end skip the arithmetic.
-// Tiles are 128 rows of one group x 128 output columns; the scheduler walks
-// (m-tile, n-tile) pairs with the m-tile index taken from the device-side
-// tile prefix, so no host synchronisation is needed for group sizes.
+// Tiles are 128 rows of one group x 256 output columns (the last tile of a row
+// block is 128 wide when N % 256 == 128); one MMA per 64-element K step is
+// 128 x 256 x 64.  On this part the tensor pipe charges per instruction rather
+// than per FLOP: an MMA costs about the same for N = 16..128 and only a third
+// more at N = 256, and every tcgen05.cp costs about as much as an MMA whatever
+// its shape.  So the kernel uses the widest MMA and moves each operand's scale
+// factors with one 128x256b copy per two K steps (A) or per K step and 256
+// rows (B), instead of one 32x128b.warpx4 copy per K step and 128 rows.  That
+// copy wants the scales already replicated the way the MMA reads them (each
+// 32-lane quarter of TMEM reads its own copy), which one warp builds in shared
+// memory from the compact 512-byte atoms of the operand chunks.
+//
+// Roles (one CTA per SM, persistent, 352 threads):
+//   warp 0      producer: per K tile the A chunk (valid-row prefix + scale
+//               atoms) and the codes + atoms of the two B chunks of the tile's
+//               256 weight rows, moved with 1-D bulk copies into a 3-deep ring.
+//               Shared memory holds only three stages, fewer than it takes to
+//               cover the memory latency at full bandwidth, so a second cursor
+//               runs PREFETCH K tiles ahead and asks L2 for the same bytes:
+//               the ring's loads then mostly hit L2.
+//   warp 1      MMA issuer: per K tile the tcgen05.cp copies of the replicated
+//               scales into the stage's TMEM scale slot, then four
+//               128x256x64 MMAs into the single 256-column TMEM accumulator.
+//               One thread issues both, so the in-order tensor pipe needs no
+//               barrier between a copy and the MMAs that read it and never
+//               idles while the next K tile's data is ready.
+//   warp 2      scale expander: copies the stage's atoms into the replicated
+//               128 x 32-byte layout (core matrices of 8 rows x 16 bytes) of
+//               one of two replica slots and signals rep_full.
+//   warps 3-10  epilogue: two warps per 32-lane TMEM quarter, 128 columns
+//               each.  They move the accumulator to registers and release it
+//               at once, so the next tile's MMAs start while they compute:
+//               scale by alpha, then store FP32/BF16 rows, or
+//               h = silu(gate) * up requantized to NVFP4 straight into the
+//               next GEMM's tiled operand.
 // Every mbarrier wait is bounded; on timeout the kernel records an error word,
 // drains what it issued, frees TMEM and returns.
 #include "internal.h"
@@ -38,39 +55,80 @@
 namespace nvf {
 namespace {
 
-constexpr int BM = 128;             // rows of A per tile (MMA M)
-constexpr int BN = 128;             // output columns per tile (MMA N)
-#ifndef NVF_GEMM_STAGES
-#define NVF_GEMM_STAGES 5
-#endif
-constexpr int STAGES = NVF_GEMM_STAGES;
-constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // A chunk + B chunk
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int STAGES = 3;
+constexpr int PREFETCH = 4;               // K tiles the L2 prefetch runs ahead of the ring
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int THREADS = 96 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SF_COL0 = 2 * BN;  // accumulators use columns [0, 256)
+constexpr uint32_t SF_COL0 = BN;          // scale slots after the accumulator
+constexpr uint32_t SF_SLOT_COLS = 64;     // A: 16 columns, B: 32 columns
 
-constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+// stage: [A chunk 18432][B codes 2 x 16384][B atoms 2 x 2048]
+constexpr int ST_A = 0;
+constexpr int ST_B = TILE_BYTES;
+constexpr int ST_BSF = ST_B + 2 * TILE_CODE_BYTES;
+constexpr int STAGE_BYTES = ST_BSF + 2 * TILE_SF_BYTES;   // 55296
+// replicated scales per stage: A 2 x 4096 (two K steps each), B 4 x 4096
+constexpr int REP_BLOCK = 4096;
+constexpr int REP_A = 0;
+constexpr int REP_B = 2 * REP_BLOCK;
+constexpr int REP_BYTES = 6 * REP_BLOCK;
+constexpr int REP_SLOTS = 2;
+
+constexpr int OFF_REP = STAGES * STAGE_BYTES;
+constexpr int OFF_BAR = OFF_REP + REP_SLOTS * REP_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + REP_SLOTS + 3;  // full, empty, rep_full, acc_full/empty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 
-static_assert(SF_COL0 + STAGES * 32 <= TMEM_COLS, "TMEM budget");
+static_assert(SF_COL0 + STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM budget");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(TILE_BYTES % 1024 == 0, "B chunk must stay 1024-byte aligned in shared memory");
+static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0 && REP_BYTES % 1024 == 0, "1024-byte alignment");
 
 struct Tile {
-  int g, mt, nt, row0, rows;
+  int g, mt, nt0, row0, rows;
+  bool wide;  // weight tiles nt0 and nt0 + 1 (256 output columns), else nt0 only
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, int ntiles) {
+// Work list of one launch.  Row block (m-tile) x 256 output columns is the
+// unit; blocks are dealt to the CTAs round-robin.  When the last round would
+// leave at least half of the CTAs idle, its blocks are split into two
+// 128-column tiles so that the round takes half as long (only when every block
+// is 256 wide, i.e. N % 256 == 0).
+struct Sched {
+  int nblocks;   // 256-column blocks per row block
+  int first_split, total;
+};
+
+__device__ __forceinline__ Sched make_sched(const GemmArgs& p) {
+  Sched s;
+  s.nblocks = (p.N + BN - 1) / BN;
+  const int blocks = __ldg(p.tile_offs + p.G) * s.nblocks;
+  const int rem = blocks % static_cast<int>(gridDim.x);
+  const int nsplit = (p.N % BN == 0 && rem > 0 && 2 * rem <= static_cast<int>(gridDim.x)) ? rem : 0;
+  s.first_split = blocks - nsplit;
+  s.total = blocks + nsplit;
+  return s;
+}
+
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sched& sc) {
   Tile x;
-  x.mt = t / ntiles;
-  x.nt = t - x.mt * ntiles;
+  int b = t, half = -1;
+  if (t >= sc.first_split) {
+    const int u = t - sc.first_split;
+    b = sc.first_split + (u >> 1);
+    half = u & 1;
+  }
+  x.mt = b / sc.nblocks;
+  const int nb = b - x.mt * sc.nblocks;
   x.g = upper_group(p.tile_offs, p.G, x.mt);
   const int local = x.mt - __ldg(p.tile_offs + x.g);
   x.row0 = __ldg(p.offsets + x.g) + local * BM;
   x.rows = min(BM, __ldg(p.offsets + x.g + 1) - x.row0);
+  x.wide = half < 0 && (nb + 1) * BN <= p.N;
+  x.nt0 = 2 * nb + (half > 0 ? 1 : 0);
   return x;
 }
 
@@ -87,6 +145,34 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
+// One 128 x 256-bit TMEM copy: lane l, column c + j receives bytes [4j, 4j+4)
+// of row l of a source stored as core matrices of 8 rows x 16 bytes: row l's
+// first 16 bytes at (l / 8) * 256 + (l % 8) * 16, its second 16 at + 128.
+__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(smem_desc(saddr, 128, 256, kSwizzleNone))
+               : "memory");
+}
+
+// Build one 4 KB replicated block from two 512-byte atoms X, Y: row l of the
+// 128 x 32-byte source = [X row l % 32 | Y row l % 32].  After the copy, lane
+// l holds X's scales of rows l % 32 + 32 c in columns c (c < 4) and Y's in
+// columns 4 + c: every lane quarter sees the same 32 x 8 words, which is how
+// the MMA reads B's scales, and lane r column r / 32 (+ 4) is A row r's.
+// 32 lanes, 64 source units of 16 bytes: two per lane, each stored 4 times.
+__device__ __forceinline__ void expand_block(uint8_t* dst, const uint8_t* x, const uint8_t* y, int lane) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int u = lane + 32 * i;         // 0..63
+    const int h = u >> 5;                // 0: X, 1: Y
+    const int j = (u >> 3) & 3;          // 8-row group within the 32 atom rows
+    const int x16 = u & 7;               // row within the group
+    const uint4 v = *reinterpret_cast<const uint4*>((h ? y : x) + j * 128 + x16 * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(dst + q * 1024 + j * 256 + h * 128 + x16 * 16) = v;
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -95,11 +181,11 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const uint32_t bar0 = s_base + OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-  auto stage_a = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
-  auto stage_b = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES + TILE_BYTES); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto repfull_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + r); };
+  const uint32_t accf_bar = bar0 + 8u * (2 * STAGES + REP_SLOTS);
+  const uint32_t acce_bar = accf_bar + 8u;
+  const uint32_t drain_mma_bar = accf_bar + 16u;
+  auto stage_addr = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -109,11 +195,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), EPI_WARPS);
-    }
-    mbar_init(drain_bar, 1);
+    for (int r = 0; r < REP_SLOTS; ++r) mbar_init(repfull_bar(r), 1);
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, EPI_WARPS);
+    mbar_init(drain_mma_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -123,38 +208,83 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const int ntiles = p.N / BN;
-  const int total = __ldg(p.tile_offs + p.G) * ntiles;
+  const int ntiles = p.N / BM;             // 128-row weight tiles per expert
   const int k64 = p.K >> 6;
   const int nkt = (k64 + 3) >> 2;
+  if (p.early_weights && threadIdx.x == 0) {
+    // The previous kernel (which produces A) may still be running: start pulling
+    // this CTA's first weight chunks into L2 meanwhile.
+    const Sched sc0 = make_sched(p);
+    int t = blockIdx.x, kt = 0;
+    for (int j = 0; j < STAGES + PREFETCH && t < sc0.total; ++j) {
+      const Tile x = decode_tile(t, p, sc0);
+      const uint8_t* bc = p.b + ((static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt + kt) * TILE_BYTES;
+      bulk_prefetch_l2(bc, TILE_BYTES);
+      if (x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, TILE_BYTES);
+      if (++kt == nkt) {
+        kt = 0;
+        t += gridDim.x;
+      }
+    }
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  const Sched sc = make_sched(p);
+  const int total = sc.total;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int stage = 0;
       uint32_t ph = 0;
-      uint32_t pending = 0, pend_par = 0;  // per-stage: load issued, parity of that phase
+      uint32_t pending = 0, pend_par = 0;  // per stage: load issued, parity of that phase
       bool ok = true;
+      // L2 prefetch cursor: (tile pf_t, K tile pf_kt), PREFETCH K tiles ahead
+      int pf_t = blockIdx.x, pf_kt = 0;
+      Tile pf_x{};
+      if (pf_t < total) pf_x = decode_tile(pf_t, p, sc);
+      auto prefetch_next = [&]() {
+        if (pf_t >= total) return;
+        const uint8_t* ac = p.a + (static_cast<size_t>(pf_x.mt) * nkt + pf_kt) * TILE_BYTES;
+        bulk_prefetch_l2(ac, static_cast<uint32_t>((pf_x.rows + 7) & ~7) * 128u);
+        bulk_prefetch_l2(ac + TILE_CODE_BYTES, TILE_SF_BYTES);
+        const uint8_t* bc = p.b + ((static_cast<size_t>(pf_x.g) * ntiles + pf_x.nt0) * nkt + pf_kt) * TILE_BYTES;
+        bulk_prefetch_l2(bc, TILE_BYTES);
+        if (pf_x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, TILE_BYTES);
+        if (++pf_kt == nkt) {
+          pf_kt = 0;
+          pf_t += gridDim.x;
+          if (pf_t < total) pf_x = decode_tile(pf_t, p, sc);
+        }
+      };
+      for (int j = 0; j < PREFETCH; ++j) prefetch_next();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile x = decode_tile(t, p, ntiles);
+        const Tile x = decode_tile(t, p, sc);
         const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
-        const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt) * nkt * TILE_BYTES;
+        const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
+        const int nbt = x.wide ? 2 : 1;
         // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
-        const uint32_t a_code_bytes = static_cast<uint32_t>(min(BM, (x.rows + 7) & ~7)) * 128u;
+        const uint32_t a_code_bytes = static_cast<uint32_t>((x.rows + 7) & ~7) * 128u;
         for (int kt = 0; kt < nkt; ++kt) {
           if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + TILE_SF_BYTES + TILE_BYTES);
+          const uint32_t st = stage_addr(stage);
+          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + TILE_SF_BYTES + nbt * TILE_BYTES);
           const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
           if (a_code_bytes == TILE_CODE_BYTES) {
-            bulk_load(stage_a(stage), ac, TILE_BYTES, full_bar(stage));
+            bulk_load(st + ST_A, ac, TILE_BYTES, full_bar(stage));
           } else {
-            bulk_load(stage_a(stage), ac, a_code_bytes, full_bar(stage));
-            bulk_load(stage_a(stage) + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
+            bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
+            bulk_load(st + ST_A + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
           }
-          bulk_load(stage_b(stage), b_chunk + static_cast<size_t>(kt) * TILE_BYTES, TILE_BYTES, full_bar(stage));
+          for (int h = 0; h < nbt; ++h) {
+            const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
+            bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
+            bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
+          }
+          prefetch_next();
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
           if (++stage == STAGES) {
@@ -172,136 +302,182 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = mxf4nvf4_idesc(BM, BN);
-      int stage = 0;
-      uint32_t ph = 0;
+      int i = 0;  // K tiles consumed so far (ring position)
+      int tile_i = 0;
       bool ok = true;
-      int i = 0;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
-        const int buf = i & 1;
-        if (!mbar_wait(acce_bar(buf), ((i >> 1) & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) break;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
+        const Tile x = decode_tile(t, p, sc);
+        const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
+        // the epilogue has moved the previous tile out of TMEM
+        if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + buf * BN;
-        for (int kt = 0; kt < nkt; ++kt) {
-          if (!mbar_wait(full_bar(stage), ph, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+        for (int kt = 0; kt < nkt; ++kt, ++i) {
+          const int s = i % STAGES;
+          const int r = i % REP_SLOTS;
+          // Stage landed and its scales are expanded.  TMEM slot s was last read by
+          // the MMAs of K tile i - 3, complete since the producer refilled stage s.
+          if (!mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t) ||
+              !mbar_wait(repfull_bar(r), (i / REP_SLOTS) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int na = min(4, k64 - kt * 4);
-          const uint32_t sfa_t = tmem + SF_COL0 + stage * 32;
-          const uint32_t sfb_t = sfa_t + 16;
-          const uint32_t a_s = stage_a(stage), b_s = stage_b(stage);
+          const uint32_t st = stage_addr(s);
+          const uint32_t sf = tmem + SF_COL0 + s * SF_SLOT_COLS;
+          const uint32_t rs = s_base + static_cast<uint32_t>(OFF_REP + r * REP_BYTES);
+          tc_copy_128x256b(sf, rs + REP_A);
+          tc_copy_128x256b(sf + 8, rs + REP_A + REP_BLOCK);
+          for (int c = 0; c < (x.wide ? 4 : 2); ++c) tc_copy_128x256b(sf + 16 + c * 8, rs + REP_B + c * REP_BLOCK);
           for (int kk = 0; kk < na; ++kk) {
-            tc_copy_sf_atom(sfa_t + kk * 4, sf_atom_desc(a_s + TILE_CODE_BYTES + kk * 512));
-            tc_copy_sf_atom(sfb_t + kk * 4, sf_atom_desc(b_s + TILE_CODE_BYTES + kk * 512));
+            const uint32_t sfa = sf + (kk >> 1) * 8 + (kk & 1) * 4;
+            const uint32_t sfb = x.wide ? sf + 16 + kk * 8 : sf + 16 + (kk >> 1) * 8 + (kk & 1) * 4;
+            tc_mma_nvfp4(tmem, operand_desc_sw128(st + ST_A + kk * 32), operand_desc_sw128(st + ST_B + kk * 32),
+                         idesc, sfa, sfb, (kt | kk) != 0 ? 1u : 0u);
           }
-          for (int kk = 0; kk < na; ++kk) {
-            tc_mma_nvfp4(d_tmem, operand_desc_sw128(a_s + kk * 32), operand_desc_sw128(b_s + kk * 32), idesc,
-                         sfa_t + kk * 4, sfb_t + kk * 4, (kt | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            ph ^= 1u;
-          }
+          tc_commit(empty_bar(s));
         }
-        if (ok) tc_commit(accf_bar(buf));
+        if (ok) tc_commit(accf_bar);
       }
-      // Every MMA / copy this thread issued must finish before TMEM is freed.
-      tc_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, p.err, -1);
+      // Every MMA this thread issued must finish before TMEM is freed.
+      tc_commit(drain_mma_bar);
+      mbar_wait_drain(drain_mma_bar, 0, p.err, -1);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------------------- scale expander
+    int i = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile x = decode_tile(t, p, sc);
+      for (int kt = 0; kt < nkt; ++kt, ++i) {
+        const int s = i % STAGES;
+        const int r = i % REP_SLOTS;
+        // Stage landed; the copies that last read replica slot r (K tile i - 2) are
+        // done (its MMAs and copies have completed).  Every lane waits (and
+        // acquires); the warp leaves together if any lane gave up.
+        bool got = mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
+        if (got && i >= REP_SLOTS)
+          got = mbar_wait(empty_bar((i - REP_SLOTS) % STAGES), ((i - REP_SLOTS) / STAGES) & 1, abort_flag, p.err,
+                          DEV_TIMEOUT_PRODUCER, t);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * STAGE_BYTES;
+        uint8_t* rep = smem + OFF_REP + r * REP_BYTES;
+        const uint8_t* a_sf = st + ST_A + TILE_CODE_BYTES;
+        const uint8_t* b_sf = st + ST_BSF;
+        // A: K steps (0,1) and (2,3) of the K tile
+        expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
+        expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
+        if (x.wide) {
+          // B, 256 rows: per K step, weight tile 0's atom and weight tile 1's
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            expand_block(rep + REP_B + kk * REP_BLOCK, b_sf + kk * 512, b_sf + TILE_SF_BYTES + kk * 512, lane);
+        } else {
+          expand_block(rep + REP_B, b_sf, b_sf + 512, lane);
+          expand_block(rep + REP_B + REP_BLOCK, b_sf + 1024, b_sf + 1536, lane);
+        }
+        // make the generic-proxy stores visible to the copies (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(repfull_bar(r));
+      }
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;       // which 64 of the tile's 128 columns
+    const int half = (warp - 3) >> 2;       // which 128 of the tile's 256 columns
     const int r = q * 32 + lane;            // tile row handled by this thread
-    int i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
-      const Tile x = decode_tile(t, p, ntiles);
-      const int buf = i & 1;
-      if (!mbar_wait(accf_bar(buf), (i >> 1) & 1, abort_flag, p.err, DEV_TIMEOUT_EPILOGUE, t)) break;
+    int tile_i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
+      const Tile x = decode_tile(t, p, sc);
+      if (!mbar_wait(accf_bar, tile_i & 1, abort_flag, p.err, DEV_TIMEOUT_EPILOGUE, t)) break;
       tc_fence_after();
-      if (q * 32 < x.rows) {
-        const uint32_t tb = tmem + buf * BN + half * 64 + (static_cast<uint32_t>(q * 32) << 16);
-        const float alpha = __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g));
-        const bool valid = r < x.rows;
-        const int64_t row = static_cast<int64_t>(x.row0) + r;
-        if constexpr (EPI == EPI_SWIGLU_QUANT) {
-          const int I = p.N >> 1;
-          const float gsq = __ldg(p.gs_q + x.g);
-          const float six_gsq = __fmul_rn(6.0f, gsq);
-          uint32_t cw[4];
-          uint32_t sfw = 0;
+      const bool active = q * 32 < x.rows && (half == 0 || x.wide);
+      uint32_t v[4][32];
+      if (active) {
+        const uint32_t tb = tmem + half * 128 + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tb + cc * 32, v);
-            tmem_ld_wait();
-            float h[16];
+        for (int c = 0; c < 4; ++c) tmem_ld32(tb + c * 32, v[c]);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar);  // accumulator is in registers: release it
+      if (!active) continue;
+      const float alpha = __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g));
+      const bool valid = r < x.rows;
+      const int64_t row = static_cast<int64_t>(x.row0) + r;
+      const int nt = x.nt0 + half;          // 128-column weight tile of this warp
+      if constexpr (EPI == EPI_SWIGLU_QUANT) {
+        // Prepared w13 rows: in every 32-column chunk c of weight tile nt, the
+        // first 16 columns are gate rows and the last 16 the matching up rows
+        // of intermediate indices nt * 64 + 16 c .. + 15.
+        const int I = p.N >> 1;
+        const float gsq = __ldg(p.gs_q + x.g);
+        const float six_gsq = __fmul_rn(6.0f, gsq);
+        uint32_t cw[8];
+        uint32_t sfw = 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              // rows past the group's end carry whatever their scale bytes held: use zeros
-              const float g = valid ? __fmul_rn(__uint_as_float(v[j]), alpha) : 0.0f;
-              const float u = valid ? __fmul_rn(__uint_as_float(v[16 + j]), alpha) : 0.0f;
-              h[j] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
-            }
-            const int c = half * 2 + cc;   // 16-wide block of this n-tile's 64 h values
-            if (p.h_dump != nullptr && valid) {
-              float4* hd = reinterpret_cast<float4*>(p.h_dump + row * I + x.nt * 64 + c * 16);
+        for (int c = 0; c < 4; ++c) {
+          float h[16];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-            }
-            sfw |= quant_block16(h, gsq, six_gsq, cw[2 * cc], cw[2 * cc + 1]) << (8 * cc);
+          for (int j = 0; j < 16; ++j) {
+            // rows past the group's end carry whatever their scale bytes held: use zeros
+            const float g = valid ? __fmul_rn(__uint_as_float(v[c][j]), alpha) : 0.0f;
+            const float u = valid ? __fmul_rn(__uint_as_float(v[c][16 + j]), alpha) : 0.0f;
+            h[j] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
           }
-          // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): this n-tile's 64
-          // h values are MMA step nt % 4 of K tile nt / 4; this warp's 32 of them
-          // are one 16-byte code chunk and two scale bytes of row r.
-          uint8_t* chunk = p.q_codes + (static_cast<size_t>(x.mt) * num_k_tiles(I) + (x.nt >> 2)) * TILE_BYTES;
-          if (valid)
-            *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, (x.nt & 3) * 32 + half * 16)) =
-                make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          *reinterpret_cast<uint16_t*>(chunk + TILE_CODE_BYTES + (x.nt & 3) * 512 +
-                                       sf_atom_offset(static_cast<uint32_t>(r), half * 2)) =
-              static_cast<uint16_t>(sfw);
-        } else {
+          if (p.h_dump != nullptr && valid) {
+            float4* hd = reinterpret_cast<float4*>(p.h_dump + row * I + nt * 64 + c * 16);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tb + cc * 32, v);
-            tmem_ld_wait();
-            if (valid) {
-              const int64_t col = static_cast<int64_t>(x.nt) * BN + half * 64 + cc * 32;
-              if constexpr (EPI == EPI_STORE_F32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.ldd + col);
+            for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+          }
+          sfw |= quant_block16(h, gsq, six_gsq, cw[2 * c], cw[2 * c + 1]) << (8 * c);
+        }
+        // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): weight tile
+        // nt's 64 h values are MMA step nt % 4 of K tile nt / 4: 32 code bytes
+        // and 4 scale bytes of row r.
+        uint8_t* chunk = p.q_codes + (static_cast<size_t>(x.mt) * num_k_tiles(I) + (nt >> 2)) * TILE_BYTES;
+        if (valid) {
+          *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, (nt & 3) * 32)) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, (nt & 3) * 32 + 16)) =
+              make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        }
+        *reinterpret_cast<uint32_t*>(chunk + TILE_CODE_BYTES + (nt & 3) * 512 + sf_atom_offset(r, 0)) = sfw;
+      } else {
+        if (valid) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  dst[j] = make_float4(__fmul_rn(__uint_as_float(v[4 * j]), alpha),
-                                       __fmul_rn(__uint_as_float(v[4 * j + 1]), alpha),
-                                       __fmul_rn(__uint_as_float(v[4 * j + 2]), alpha),
-                                       __fmul_rn(__uint_as_float(v[4 * j + 3]), alpha));
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
+          for (int c = 0; c < 4; ++c) {
+            const int64_t col = static_cast<int64_t>(nt) * 128 + c * 32;
+            if constexpr (EPI == EPI_STORE_F32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.ldd + col);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint32_t w[4];
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__fmul_rn(__uint_as_float(v[c][4 * j]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 1]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 2]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
 #pragma unroll
-                  for (int h2 = 0; h2 < 4; ++h2) {
-                    __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * j + 2 * h2]), alpha),
-                                                             __fmul_rn(__uint_as_float(v[8 * j + 2 * h2 + 1]), alpha));
-                    w[h2] = *reinterpret_cast<uint32_t*>(&b);
-                  }
-                  dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w[4];
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                  __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2]), alpha),
+                                                           __fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2 + 1]), alpha));
+                  w[h2] = *reinterpret_cast<uint32_t*>(&b);
                 }
+                dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));
     }
   }
 
@@ -316,8 +492,8 @@ cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
   auto k = grouped_gemm_kernel<EPI>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k<<<grid, THREADS, SMEM_BYTES, s>>>(a);
-  return cudaGetLastError();
+  prefer_max_shared(reinterpret_cast<const void*>(k));
+  return launch_kernel(k, dim3(grid), dim3(THREADS), SMEM_BYTES, s, a.pdl, a);
 }
 
 }  // namespace
@@ -325,7 +501,7 @@ cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** why) {
   *why = nullptr;
   if (a.a_rows <= 0) return cudaSuccess;
-  const int64_t max_tiles = ((a.a_rows + BM - 1) / BM + a.G) * (a.N / BN);
+  const int64_t max_tiles = ((a.a_rows + BM - 1) / BM + a.G) * ((a.N + BN - 1) / BN);
   int grid = a.max_ctas > 0 ? a.max_ctas : sm_count();
   if (grid > max_tiles) grid = static_cast<int>(max_tiles);
   if (grid < 1) grid = 1;

@@ -9,6 +9,26 @@ namespace nvf {
 
 enum XDtype : int { X_F32 = 0, X_BF16 = 1 };
 
+// Launch `kernel` on stream `s`.  With `pdl` the launch is a programmatic
+// dependent launch: it may begin while the previous kernel of the stream is
+// still running, and the kernel executes griddep_wait() before it touches
+// anything that kernel (or an earlier one) wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct QuantArgs {
   const void* x;            // [src_rows, ldx] f32 or bf16
   int x_dtype;
@@ -39,16 +59,22 @@ struct RouteArgs {
   int32_t* perm_to_src;     // [R']
   int32_t* src_to_perm;     // [R']
   int32_t* perm_token;      // [R']
-  int32_t* chunk_counts;    // workspace [nchunks, E]
-  int32_t* chunk_base;      // workspace [nchunks, E]
+  uint32_t* words;          // scratch [ceil(T/32), E]: bit i of words[w][e]: token 32w+i chose e
+  int32_t* prefix;          // scratch [ceil(T/32), E]: earlier tokens that chose e (many tokens only)
+  int32_t* counts;          // scratch [E]
+  // Optional activation quantization done by the permute kernel (A1 of the forward pass):
+  const void* x;            // nullable bf16 [T, H]
+  int32_t H;
+  const float* gs_a1;       // [E']
+  uint8_t* a1;              // TILED_GROUPED operand, K = H
+  bool pdl;                 // first kernel as a programmatic dependent launch
 };
-int route_tokens_per_chunk(int32_t T);
-int route_num_chunks(int32_t T);
+size_t route_scratch_bytes(int32_t T, int32_t E);
 int route_kernel_launches(int32_t T, int32_t k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
-                           int32_t k, int32_t shared, int out_dtype, void* out, cudaStream_t s);
+                           int32_t k, int32_t shared, int out_dtype, void* out, cudaStream_t s, bool pdl);
 
 enum GemmEpilogue : int { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_SWIGLU_QUANT = 2 };
 
@@ -69,10 +95,17 @@ struct GemmArgs {
   float* h_dump;            // SWIGLU: nullable [a_rows, N/2]
   int* err;                 // device error word
   int max_ctas;             // 0: one CTA per SM
+  bool pdl;                 // programmatic dependent launch
+  // offsets / tile_offs were complete before the preceding kernel began, so the
+  // producer may start pulling weights into L2 before its dependency wait
+  bool early_weights;
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** why);
 
 int* device_error_word();   // per current device, nullptr on failure
 int sm_count();
+// Ask for the largest shared-memory carveout once per (device, kernel), so that
+// consecutive kernels of the layer do not reconfigure L1 / shared memory.
+void prefer_max_shared(const void* func);
 
 }  // namespace nvf

@@ -42,6 +42,17 @@ __device__ __forceinline__ void report_error(int* err, int code, int detail) {
   if (err != nullptr && atomicCAS(err, 0, code) == 0) err[1] = detail;
 }
 
+// ----------------------------------------------------------------------------- dependent launch
+// With programmatic dependent launch a kernel may start while the previous
+// kernel in the stream is still running.  griddep_wait() blocks until that
+// kernel has completed and its writes are visible (a no-op when the kernel was
+// launched normally); griddep_launch_dependents() lets the next kernel start
+// once every CTA of this one has executed it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -104,6 +115,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// Hint: start moving [src, src + bytes) from memory into L2 (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ----------------------------------------------------------------------------- tcgen05

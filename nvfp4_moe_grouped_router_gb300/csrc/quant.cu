@@ -115,6 +115,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s) {
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
   const size_t smem = (a.offsets && a.G < kMaxSmemGroups) ? 2 * (a.G + 1) * sizeof(int32_t) : 0;
+  prefer_max_shared(reinterpret_cast<const void*>(quantize_kernel));
   quantize_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(a);
   return cudaGetLastError();
 }

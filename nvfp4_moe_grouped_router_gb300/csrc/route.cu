@@ -1,35 +1,45 @@
 // Routing, permutation and combine kernels.
 //
-//   route_topk    : one warp per token: top-k of (logit + bias) by repeated warp
-//                   argmax (ties to the lower expert id), softmax over the k
-//                   selected (renormalised) or over all E, and a per-chunk
-//                   expert histogram.
-//   route_scan    : one CTA: per-expert totals, exclusive prefix -> expert
-//                   offsets, prefix of ceil(m_e / 128) -> tile offsets, and the
-//                   first output slot of every (chunk, expert).
-//   route_scatter : one warp per chunk walks its assignments a = t*k + j in
-//                   order and places each at offsets[e] + rank, which makes the
-//                   permutation a stable sort by expert (deterministic, no
-//                   global atomics).
-//   combine       : out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ shared row).
+//   route_topk_bits : one warp per token: top-k of (logit + bias) by repeated
+//                     warp argmax (ties to the lower expert id) and a softmax
+//                     over the k selected (renormalised) or over all E.  Each
+//                     CTA owns 32 consecutive tokens and writes, for every
+//                     expert e, one 32-bit word whose bit i says that token
+//                     32*blockIdx + i chose e.
+//   route_prefix    : (many tokens only) per expert, exclusive prefix of the
+//                     popcounts of its words: how many earlier tokens chose it.
+//   route_permute   : every CTA scans the per-expert counts (expert offsets and
+//                     the 128-row tile prefix); then one warp per token places
+//                     each of its assignments at offsets[e] + (number of earlier
+//                     tokens that chose e).  A token picks k distinct experts,
+//                     so this is exactly the stable order of assignments
+//                     a = t*k + j by expert -- computed in parallel, without
+//                     atomics, deterministically.  With activations given,
+//                     one warp per (token, slot) quantizes the token's row
+//                     with the slot's expert global scale into that slot of
+//                     the gate_up GEMM's TILED_GROUPED operand.
+//   combine         : out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ shared row).
 //
 // Sources: top-k routing over many routed experts plus one shared expert
 // (FlashInfer issue #2723, "Model" table: 512 routed + 1 shared, 10 routed per
 // token); per-expert problem sizes / offsets feeding the grouped GEMM (vLLM PR
 // #29242, commit "Fix get_cutlass_moe_mm_data not compiling" and the review
-// of nvfp4_blockwise_moe_kernel.cu naming num_experts, M, N, K).
+// of nvfp4_blockwise_moe_kernel.cu naming num_experts, M, N, K); BF16 -> FP4
+// per-token activation quantization (FlashInfer issue #2723, "Why 39 vs 49
+// tok/s?").
 #include "internal.h"
 #include "layout.cuh"
 #include "ptx.cuh"
+#include "quant_block.cuh"
 
 #include <cuda_bf16.h>
 
 namespace nvf {
 namespace {
 
-constexpr int kMaxE = 1024;            // routed experts
-constexpr int kPerLane = kMaxE / 32;   // logits held per lane
-constexpr int kTopkWarps = 8;
+constexpr int kMaxE = 1024;          // routed experts
+constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
+constexpr int kPermWarps = 16;       // tokens per permute CTA
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -99,20 +109,49 @@ __device__ __forceinline__ int topk_token(const RouteArgs& a, int t, int lane) {
 }
 
 template <int NV>
-__global__ void __launch_bounds__(kTopkWarps * 32) route_topk_kernel(RouteArgs a, int tpc) {
-  extern __shared__ int hist[];  // [E]
+constexpr int topk_threads() { return NV <= 8 ? 1024 : 512; }
+
+template <int NV>
+__global__ void __launch_bounds__(topk_threads<NV>()) route_topk_bits_kernel(RouteArgs a) {
+  extern __shared__ uint32_t s_words[];  // [E]
+  griddep_wait();
+  griddep_launch_dependents();
   const int E = a.E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_words[e] = 0;
   __syncthreads();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * tpc;
-  const int t1 = min(a.T, t0 + tpc);
-  for (int t = t0 + warp; t < t1; t += kTopkWarps) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int t0 = blockIdx.x * 32;
+  for (int i = warp; i < 32; i += nwarps) {
+    const int t = t0 + i;
+    if (t >= a.T) break;
     const int e = topk_token<NV>(a, t, lane);
-    if (e >= 0) atomicAdd(&hist[e], 1);
+    if (e >= 0) atomicOr(&s_words[e], 1u << i);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) a.words[static_cast<int64_t>(blockIdx.x) * E + e] = s_words[e];
+}
+
+// One warp per expert: exclusive prefix over word columns of the popcounts.
+__global__ void __launch_bounds__(256) route_prefix_kernel(RouteArgs a, int W) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= a.E) return;
+  int carry = 0;
+  for (int w0 = 0; w0 < W; w0 += 32) {
+    const int w = w0 + lane;
+    const int c = w < W ? __popc(a.words[static_cast<int64_t>(w) * a.E + e]) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (w < W) a.prefix[static_cast<int64_t>(w) * a.E + e] = carry + incl - c;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) a.counts[e] = carry;
 }
 
 // Exclusive scan over n <= 2048 values held in smem by one warp; returns the total.
@@ -136,76 +175,110 @@ __device__ int warp_exclusive_scan(int* vals, int n, int lane) {
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(RouteArgs a, int nchunks) {
-  __shared__ int cnt[kMaxE + 1];
-  __shared__ int til[kMaxE + 1];
-  const int E = a.E, Et = a.E + a.shared;
-  for (int e = threadIdx.x; e < Et; e += blockDim.x) {
-    int total = 0;
-    if (e < E) {
-      for (int c = 0; c < nchunks; ++c) {
-        const int64_t i = static_cast<int64_t>(c) * E + e;
-        const int v = a.chunk_counts[i];
-        a.chunk_base[i] = total;
-        total += v;
-      }
-    } else {
-      total = a.T;  // the shared expert sees every token
-    }
-    cnt[e] = total;
-    til[e] = (total + 127) >> 7;
+// Stable position of assignment (t, j) in the expert-sorted order, and the
+// expert it goes to (the shared expert's slot j == k sits after all routed rows).
+__device__ __forceinline__ int assignment_pos(const RouteArgs& a, const int* offs, int W, int t, int j, int& e) {
+  if (j == a.k) {
+    e = a.E;
+    return a.T * a.k + t;
   }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int tot = warp_exclusive_scan(cnt, Et, threadIdx.x);
-    const int ttot = warp_exclusive_scan(til, Et, threadIdx.x);
-    if (threadIdx.x == 0) {
-      a.offsets[Et] = tot;
-      a.tile_offs[Et] = ttot;
-    }
+  e = a.ids[static_cast<int64_t>(t) * a.k + j];
+  const int wc = t >> 5;
+  const uint32_t below = (1u << (t & 31)) - 1u;
+  int rank = __popc(a.words[static_cast<int64_t>(wc) * a.E + e] & below);
+  if (W <= kInlineWords) {
+    for (int w = 0; w < wc; ++w) rank += __popc(a.words[static_cast<int64_t>(w) * a.E + e]);
+  } else {
+    rank += a.prefix[static_cast<int64_t>(wc) * a.E + e];
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < Et; e += blockDim.x) {
-    a.offsets[e] = cnt[e];
-    a.tile_offs[e] = til[e];
-  }
-  for (int64_t i = threadIdx.x; i < static_cast<int64_t>(nchunks) * E; i += blockDim.x)
-    a.chunk_base[i] += cnt[i % E];
+  return offs[e] + rank;
 }
 
-__global__ void __launch_bounds__(32) route_scatter_kernel(RouteArgs a, int tpc) {
-  extern __shared__ int next[];  // [E]: next free slot of each expert for this chunk
-  const int E = a.E, k = a.k, lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) next[e] = a.chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
-  __syncwarp();
-  const int t0 = blockIdx.x * tpc;
-  const int t1 = min(a.T, t0 + tpc);
-  const int64_t a0 = static_cast<int64_t>(t0) * k, a1 = static_cast<int64_t>(t1) * k;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int64_t base = a0; base < a1; base += 32) {
-    const int64_t as = base + lane;
-    const bool active = as < a1;
-    const uint32_t mask = __ballot_sync(0xffffffffu, active);
-    int e = 0;
-    uint32_t peers = 0;
-    if (active) {
-      e = a.ids[as];
-      peers = __match_any_sync(mask, e);
-      const int pos = next[e] + __popc(peers & lt);
-      a.perm_to_src[pos] = static_cast<int32_t>(as);
-      a.src_to_perm[as] = pos;
-      a.perm_token[pos] = static_cast<int32_t>(as / k);
+// Grid (ceil(T / kPermWarps), slots) with activations (QUANT): warp w of CTA
+// (bx, j) places assignment (t = bx * kPermWarps + w, j) and quantizes token
+// t's row into that slot, one 64-element group per lane.  Without activations
+// the grid is (ceil(T / kPermWarps), 1) and lane j of a warp places slot j.
+template <bool QUANT>
+__global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArgs a, int W) {
+  __shared__ int offs[kMaxE + 2];
+  __shared__ int til[kMaxE + 2];
+  const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  griddep_wait();
+  griddep_launch_dependents();
+  // per-expert counts -> expert offsets and tile offsets (every CTA, redundantly)
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) {
+    int c;
+    if (e == E) {
+      c = T;  // the shared expert sees every token
+    } else if (W <= kInlineWords) {
+      c = 0;
+      for (int w = 0; w < W; ++w) c += __popc(a.words[static_cast<int64_t>(w) * E + e]);
+    } else {
+      c = a.counts[e];
     }
-    __syncwarp();
-    if (active && lane == 31 - __clz(peers)) next[e] += __popc(peers);
-    __syncwarp();
+    offs[e] = c;
+    til[e] = (c + 127) >> 7;
   }
-  if (a.shared) {
-    const int64_t R = static_cast<int64_t>(a.T) * k;
-    for (int t = t0 + lane; t < t1; t += 32) {
-      a.perm_to_src[R + t] = static_cast<int32_t>(R + t);
-      a.src_to_perm[R + t] = static_cast<int32_t>(R + t);
-      a.perm_token[R + t] = t;
+  __syncthreads();
+  if (warp == 0) {
+    const int tot = warp_exclusive_scan(offs, Et, lane);
+    const int ttot = warp_exclusive_scan(til, Et, lane);
+    if (lane == 0) {
+      offs[Et] = tot;
+      til[Et] = ttot;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int e = threadIdx.x; e <= Et; e += blockDim.x) {
+      a.offsets[e] = offs[e];
+      a.tile_offs[e] = til[e];
+    }
+  }
+  const int t = blockIdx.x * kPermWarps + warp;
+  if (t >= T) return;
+  if constexpr (!QUANT) {
+    if (lane < k + a.shared) {
+      int e;
+      const int pos = assignment_pos(a, offs, W, t, lane, e);
+      const int as = lane < k ? t * k + lane : pos;
+      a.perm_to_src[pos] = as;
+      a.src_to_perm[as] = pos;
+      a.perm_token[pos] = t;
+    }
+  } else {
+    const int j = blockIdx.y;
+    int e;
+    const int pos = assignment_pos(a, offs, W, t, j, e);
+    if (lane == 0) {
+      const int as = j < k ? t * k + j : pos;
+      a.perm_to_src[pos] = as;
+      a.src_to_perm[as] = pos;
+      a.perm_token[pos] = t;
+    }
+    const float gs = __ldg(a.gs_a1 + e);
+    const int local = pos - offs[e];
+    const int tile = til[e] + (local >> 7);
+    const int gpr = a.H >> 6;
+    for (int gg = lane; gg < gpr; gg += 32) {
+      float v[64];
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                        static_cast<int64_t>(t) * a.H + gg * 64);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 u = __ldg(src + i);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[i * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
+          v[i * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+        }
+      }
+      uint32_t w[8];
+      const uint32_t sf = quant_group64(v, gs, w);
+      store_group64(a.a1, nullptr, LAYOUT_TILED_GROUPED, a.H, pos, tile, static_cast<uint32_t>(local & 127), gg, w,
+                    sf);
     }
   }
 }
@@ -214,6 +287,7 @@ template <int OUT_BF16>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
                                                      void* out) {
+  griddep_wait();
   const int h4 = H >> 2;
   const int64_t total = static_cast<int64_t>(T) * h4;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -247,105 +321,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
-}  // namespace
-
-int route_tokens_per_chunk(int32_t T) {
-  int tpc = 64;
-  while ((T + tpc - 1) / tpc > 2048) tpc *= 2;
-  return tpc;
-}
-int route_num_chunks(int32_t T) {
-  const int tpc = route_tokens_per_chunk(T);
-  return T == 0 ? 0 : (T + tpc - 1) / tpc;
-}
-
-namespace {
-
-constexpr int kSmallAssign = 4096;   // T*k handled by the single-CTA path
-
-// Small batches: top-k, histogram, prefix sums and the stable scatter in one
-// CTA of 32 warps: one launch, no scratch memory.
-template <int NV>
-__global__ void __launch_bounds__(1024) route_small_kernel(RouteArgs a) {
-  __shared__ int cnt[kMaxE + 1];
-  __shared__ int til[kMaxE + 1];
-  __shared__ int s_ids[kSmallAssign];
-  const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = threadIdx.x; e < Et; e += blockDim.x) cnt[e] = (e < E) ? 0 : T;  // shared expert: every token
-  __syncthreads();
-  for (int t = warp; t < T; t += 32) {
-    const int e = topk_token<NV>(a, t, lane);
-    if (e >= 0) {
-      s_ids[t * k + lane] = e;
-      atomicAdd(&cnt[e], 1);
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    for (int e = lane; e < Et; e += 32) til[e] = (cnt[e] + 127) >> 7;
-    __syncwarp();
-    const int tot = warp_exclusive_scan(cnt, Et, lane);
-    const int ttot = warp_exclusive_scan(til, Et, lane);
-    __syncwarp();
-    for (int e = lane; e < Et; e += 32) {
-      a.offsets[e] = cnt[e];
-      a.tile_offs[e] = til[e];
-    }
-    if (lane == 0) {
-      a.offsets[Et] = tot;
-      a.tile_offs[Et] = ttot;
-    }
-    // Stable scatter in assignment order; cnt[e] is now expert e's next free slot.
-    const int R = T * k;
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int base = 0; base < R; base += 32) {
-      const int as = base + lane;
-      const bool active = as < R;
-      const uint32_t mask = __ballot_sync(0xffffffffu, active);
-      int e = 0;
-      uint32_t peers = 0;
-      if (active) {
-        e = s_ids[as];
-        peers = __match_any_sync(mask, e);
-        const int pos = cnt[e] + __popc(peers & lt);
-        a.perm_to_src[pos] = as;
-        a.src_to_perm[as] = pos;
-        a.perm_token[pos] = as / k;
-      }
-      __syncwarp();
-      if (active && lane == 31 - __clz(peers)) cnt[e] += __popc(peers);
-      __syncwarp();
-    }
-  }
-  if (a.shared) {
-    const int R = T * k;
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
-      a.perm_to_src[R + t] = R + t;
-      a.src_to_perm[R + t] = R + t;
-      a.perm_token[R + t] = t;
-    }
-  }
-}
-
 template <int NV>
 cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
-  if (static_cast<int64_t>(a.T) * a.k <= kSmallAssign) {
-    route_small_kernel<NV><<<1, 1024, 0, s>>>(a);
-    return cudaGetLastError();
+  const int W = (a.T + 31) / 32;
+  // the first kernel follows the caller's choice; the others always depend
+  // programmatically on the kernel before them
+  bool pdl = a.pdl;
+  cudaError_t e = cudaSuccess;
+  if (W > 0) {
+    auto kt = route_topk_bits_kernel<NV>;
+    prefer_max_shared(reinterpret_cast<const void*>(kt));
+    e = launch_kernel(kt, dim3(W), dim3(topk_threads<NV>()), a.E * sizeof(uint32_t), s, pdl, a);
+    if (e != cudaSuccess) return e;
+    pdl = true;
+    if (W > kInlineWords) {
+      e = launch_kernel(route_prefix_kernel, dim3((a.E + 7) / 8), dim3(256), 0, s, pdl, a, W);
+      if (e != cudaSuccess) return e;
+    }
   }
-  const int tpc = route_tokens_per_chunk(a.T);
-  const int nch = route_num_chunks(a.T);
-  route_topk_kernel<NV><<<nch, kTopkWarps * 32, a.E * sizeof(int), s>>>(a, tpc);
-  route_scan_kernel<<<1, 1024, 0, s>>>(a, nch);
-  route_scatter_kernel<<<nch, 32, a.E * sizeof(int), s>>>(a, tpc);
-  return cudaGetLastError();
+  const int blocks = a.T > 0 ? (a.T + kPermWarps - 1) / kPermWarps : 1;
+  if (a.x != nullptr) {
+    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<true>));
+    e = launch_kernel(route_permute_kernel<true>, dim3(blocks, a.k + a.shared), dim3(kPermWarps * 32), 0, s, pdl, a,
+                      W);
+  } else {
+    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<false>));
+    e = launch_kernel(route_permute_kernel<false>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
+  }
+  return e;
 }
 
 }  // namespace
 
+size_t route_scratch_bytes(int32_t T, int32_t E) {
+  const size_t W = (static_cast<size_t>(T) + 31) / 32;
+  return (2 * W * E + E) * sizeof(int32_t);
+}
+
 int route_kernel_launches(int32_t T, int32_t k) {
-  return static_cast<int64_t>(T) * k <= kSmallAssign ? 1 : 3;
+  (void)k;
+  const int W = (T + 31) / 32;
+  return W == 0 ? 1 : (W > kInlineWords ? 3 : 2);
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -356,17 +372,15 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,
-                           int32_t shared, int out_dtype, void* out, cudaStream_t s) {
+                           int32_t shared, int out_dtype, void* out, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int64_t total = static_cast<int64_t>(T) * (H / 4);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
-  if (out_dtype == X_BF16)
-    combine_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(y, H, weights, s2p, T, k, shared, out);
-  else
-    combine_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, s>>>(y, H, weights, s2p, T, k, shared, out);
-  return cudaGetLastError();
+  prefer_max_shared(reinterpret_cast<const void*>(out_dtype == X_BF16 ? combine_kernel<1> : combine_kernel<0>));
+  return launch_kernel(out_dtype == X_BF16 ? combine_kernel<1> : combine_kernel<0>, dim3(static_cast<unsigned>(blocks)),
+                       dim3(256), 0, s, pdl, y, H, weights, s2p, T, k, shared, out);
 }
 
 }  // namespace nvf

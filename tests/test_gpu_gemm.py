@@ -119,6 +119,30 @@ def test_random_within_tolerance(nvf, sizes, N, K, out_dtype):
         assert np.all(np.abs(D - ref) <= TOL * rms + np.abs(ref) * 2.0 ** -8)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_split_last_round(nvf, out_dtype):
+    """Few row blocks and a large row capacity: the launch gets one CTA per SM
+    and every 256-column block is split into two 128-column tiles (the kernel
+    halves the last round when it would leave most CTAs idle)."""
+    rng = np.random.default_rng(11)
+    sizes = [5, 7, 130, 0, 64]
+    G, N, K = len(sizes), 512, 320
+    R = sum(sizes)
+    a = rng.standard_normal((R, K)).astype(np.float32)
+    gs_a = np.full(G, F.global_scale(np.abs(a).max()), np.float32)
+    a_c, a_s = F.quantize_rows(a, gs_a[0])
+    w = (rng.standard_normal((G, N, K)) * 0.02).astype(np.float32)
+    qw = [M.quantize_expert_weights(w[g]) for g in range(G)]
+    w_c = np.stack([q[0] for q in qw])
+    w_s = np.stack([q[1] for q in qw])
+    gs_w = np.array([q[2] for q in qw], np.float32)
+    D, offs = _run(nvf, a_c, a_s, sizes, w_c, w_s, gs_a, gs_w, out_dtype, pad_rows=30000)
+    ref = M.grouped_gemm(a_c, a_s, offs, gs_a, w_c, w_s, gs_w)
+    rms = np.sqrt(np.mean(ref ** 2))
+    bound = TOL * rms + (np.abs(ref) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0)
+    assert np.all(np.abs(D - ref) <= bound)
+
+
 def test_argument_validation(nvf):
     z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     f = torch.ones(1, dtype=torch.float32, device="cuda")
