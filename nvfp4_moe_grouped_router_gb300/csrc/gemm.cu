@@ -17,13 +17,14 @@
 // factors with one 128x256b copy per two K steps (A) or per K step and 256
 // rows (B), instead of one 32x128b.warpx4 copy per K step and 128 rows.  That
 // copy wants the scales already replicated the way the MMA reads them (each
-// 32-lane quarter of TMEM reads its own copy), which one warp builds in shared
+// 32-lane quarter of TMEM reads its own copy), which two warps build in shared
 // memory from the compact 512-byte atoms of the operand chunks.
 //
-// Roles (one CTA per SM, persistent, 352 threads):
-//   warp 0      producer: per K tile the A chunk (valid-row prefix + scale
-//               atoms) and the codes + atoms of the two B chunks of the tile's
-//               256 weight rows, moved with 1-D bulk copies into a 3-deep ring.
+// Roles (one CTA per SM, persistent, 384 threads):
+//   warp 0      producer: per K tile the scale atoms of the A chunk and of the
+//               two B chunks of the tile's 256 weight rows (first, on their own
+//               barrier), then the A codes (valid-row prefix) and the B codes,
+//               moved with 1-D bulk copies into a 3-deep ring.
 //               Shared memory holds only three stages, fewer than it takes to
 //               cover the memory latency at full bandwidth, so a second cursor
 //               runs PREFETCH K tiles ahead and asks L2 for the same bytes:
@@ -34,10 +35,12 @@
 //               One thread issues both, so the in-order tensor pipe needs no
 //               barrier between a copy and the MMAs that read it and never
 //               idles while the next K tile's data is ready.
-//   warp 2      scale expander: copies the stage's atoms into the replicated
+//   warps 2-3   scale expanders: as soon as a stage's atoms have landed (while
+//               its codes are still arriving), copy them into the replicated
 //               128 x 32-byte layout (core matrices of 8 rows x 16 bytes) of
-//               one of two replica slots and signals rep_full.
-//   warps 3-10  epilogue: two warps per 32-lane TMEM quarter, 128 columns
+//               one of two replica slots, half of the blocks each, and signal
+//               rep_full.
+//   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, 128 columns
 //               each.  They move the accumulator to registers and release it
 //               at once, so the next tile's MMAs start while they compute:
 //               scale by alpha, then store FP32/BF16 rows, or
@@ -60,7 +63,8 @@ constexpr int BN = 256;
 constexpr int STAGES = 3;
 constexpr int PREFETCH = 4;               // K tiles the L2 prefetch runs ahead of the ring
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 96 + 32 * EPI_WARPS;
+constexpr int EXP_WARPS = 2;
+constexpr int THREADS = 64 + 32 * EXP_WARPS + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = BN;          // scale slots after the accumulator
 constexpr uint32_t SF_SLOT_COLS = 64;     // A: 16 columns, B: 32 columns
@@ -79,7 +83,7 @@ constexpr int REP_SLOTS = 2;
 
 constexpr int OFF_REP = STAGES * STAGE_BYTES;
 constexpr int OFF_BAR = OFF_REP + REP_SLOTS * REP_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + REP_SLOTS + 3;  // full, empty, rep_full, acc_full/empty, drain
+constexpr int NUM_BARS = 3 * STAGES + REP_SLOTS + 3;  // full, empty, sf_full, rep_full, acc_full/empty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 
@@ -181,8 +185,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const uint32_t bar0 = s_base + OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto repfull_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + r); };
-  const uint32_t accf_bar = bar0 + 8u * (2 * STAGES + REP_SLOTS);
+  auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto repfull_bar = [&](int r) { return bar0 + 8u * (3 * STAGES + r); };
+  const uint32_t accf_bar = bar0 + 8u * (3 * STAGES + REP_SLOTS);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_mma_bar = accf_bar + 16u;
   auto stage_addr = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
@@ -194,8 +199,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sffull_bar(s), 1);
     }
-    for (int r = 0; r < REP_SLOTS; ++r) mbar_init(repfull_bar(r), 1);
+    for (int r = 0; r < REP_SLOTS; ++r) mbar_init(repfull_bar(r), EXP_WARPS);
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, EPI_WARPS);
     mbar_init(drain_mma_bar, 1);
@@ -271,18 +277,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             break;
           }
           const uint32_t st = stage_addr(stage);
-          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + TILE_SF_BYTES + nbt * TILE_BYTES);
           const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
-          if (a_code_bytes == TILE_CODE_BYTES) {
-            bulk_load(st + ST_A, ac, TILE_BYTES, full_bar(stage));
-          } else {
-            bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
-            bulk_load(st + ST_A + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
+          // scale atoms first: the expanders start on them while the codes arrive
+          mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
+          bulk_load(st + ST_A + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
+          for (int h = 0; h < nbt; ++h) {
+            const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
+            bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
           }
+          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + nbt * TILE_CODE_BYTES);
+          bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
           for (int h = 0; h < nbt; ++h) {
             const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
             bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
-            bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, full_bar(stage));
           }
           prefetch_next();
           pending |= 1u << stage;
@@ -296,7 +303,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       if (!ok || *abort_flag) {
         // Let every copy this thread issued land before the CTA goes away.
         for (int s = 0; s < STAGES; ++s)
-          if ((pending >> s) & 1u) mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
+          if ((pending >> s) & 1u) {
+            mbar_wait_drain(sffull_bar(s), (pend_par >> s) & 1u, p.err, s);
+            mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
+          }
       }
     }
   } else if (warp == 1) {
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       tc_commit(drain_mma_bar);
       mbar_wait_drain(drain_mma_bar, 0, p.err, -1);
     }
-  } else if (warp == 2) {
+  } else if (warp < 2 + EXP_WARPS) {
     // -------------------------------------------------------------- scale expander
     int i = 0;
     bool ok = true;
@@ -352,10 +362,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       for (int kt = 0; kt < nkt; ++kt, ++i) {
         const int s = i % STAGES;
         const int r = i % REP_SLOTS;
-        // Stage landed; the copies that last read replica slot r (K tile i - 2) are
+        // The stage's atoms landed; the copies that last read replica slot r (K tile i - 2) are
         // done (its MMAs and copies have completed).  Every lane waits (and
         // acquires); the warp leaves together if any lane gave up.
-        bool got = mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
+        bool got = mbar_wait(sffull_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
         if (got && i >= REP_SLOTS)
           got = mbar_wait(empty_bar((i - REP_SLOTS) % STAGES), ((i - REP_SLOTS) / STAGES) & 1, abort_flag, p.err,
                           DEV_TIMEOUT_PRODUCER, t);
@@ -367,14 +377,21 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         uint8_t* rep = smem + OFF_REP + r * REP_BYTES;
         const uint8_t* a_sf = st + ST_A + TILE_CODE_BYTES;
         const uint8_t* b_sf = st + ST_BSF;
-        // A: K steps (0,1) and (2,3) of the K tile
-        expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
-        expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
         if (x.wide) {
-          // B, 256 rows: per K step, weight tile 0's atom and weight tile 1's
+          // A: K steps (0,1) and (2,3); B, 256 rows: per K step, weight tile 0's
+          // atom and weight tile 1's.  Expander 0 takes A and B step 0.
+          if (warp == 2) {
+            expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
+            expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
+            expand_block(rep + REP_B, b_sf, b_sf + TILE_SF_BYTES, lane);
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            expand_block(rep + REP_B + kk * REP_BLOCK, b_sf + kk * 512, b_sf + TILE_SF_BYTES + kk * 512, lane);
+            for (int kk = 1; kk < 4; ++kk)
+              expand_block(rep + REP_B + kk * REP_BLOCK, b_sf + kk * 512, b_sf + TILE_SF_BYTES + kk * 512, lane);
+          }
+        } else if (warp == 2) {
+          expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
+          expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
         } else {
           expand_block(rep + REP_B, b_sf, b_sf + 512, lane);
           expand_block(rep + REP_B + REP_BLOCK, b_sf + 1024, b_sf + 1536, lane);
@@ -388,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 3) >> 2;       // which 128 of the tile's 256 columns
+    const int half = (warp - 2 - EXP_WARPS) >> 2;  // which 128 of the tile's 256 columns
     const int r = q * 32 + lane;            // tile row handled by this thread
     int tile_i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
