@@ -217,6 +217,7 @@ typedef struct nvf_moe_weights {
 typedef struct nvf_moe_ws_layout {
   size_t topk_ids, topk_w, expert_offsets, tile_offsets, perm_to_src, src_to_perm, perm_token;
   size_t route_scratch;
+  size_t tile_group;        /* int32[R/128 + E' + 1]: expert of each 128-row tile of A1 / A2 */
   size_t a1;                /* NVF_LAYOUT_TILED_GROUPED, K = H */
   size_t a2;                /* NVF_LAYOUT_TILED_GROUPED, K = I */
   size_t y;                 /* float[R, H], row = permuted slot */
@@ -235,9 +236,11 @@ nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I
  *   ws       device scratch of nvfp4_moe_workspace_layout().total bytes, 256-byte aligned.
  *   stage_events NULL, or NVF_MOE_STAGE_EVENTS cudaEvent_t handles recorded on `stream`
  *            before routing and after each stage (route+permute, activation quant,
- *            gate_up GEMM, down GEMM, combine), for per-stage timing; small
- *            batches route and quantize in one kernel, and then the events
- *            after routing and after quantization are recorded together. */
+ *            gate_up GEMM, down GEMM, combine), for per-stage timing.  The
+ *            permutation kernel quantizes the activations, so the events after
+ *            routing and after quantization are recorded together.  With events
+ *            the kernels run one after the other; without, each kernel after
+ *            the first may start while its predecessor finishes. */
 #define NVF_MOE_STAGE_EVENTS 6
 nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
                              int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,

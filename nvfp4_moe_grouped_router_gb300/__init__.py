@@ -58,7 +58,7 @@ class MoEWeightsC(ctypes.Structure):
 
 class WorkspaceLayoutC(ctypes.Structure):
     _fields_ = [(n, _SZ) for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src",
-                                    "src_to_perm", "perm_token", "route_scratch", "a1", "a2", "y",
+                                    "src_to_perm", "perm_token", "route_scratch", "tile_group", "a1", "a2", "y",
                                     "total")] + [("R", _I64)]
 
 

@@ -328,6 +328,7 @@ nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I
   size_t rs = 0;
   moe_route_permute_workspace_size(T, E, &rs);
   L->route_scratch = take(rs);
+  L->tile_group = take(sizeof(int32_t) * (static_cast<size_t>(R) / 128 + Et + 1));
   L->a1 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), H));
   L->a2 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), I));
   L->y = take(sizeof(float) * static_cast<size_t>(R) * H);
@@ -377,6 +378,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   ra.H = H;
   ra.gs_a1 = gs_a1;
   ra.a1 = base + L.a1;
+  ra.tile_group = i32(L.tile_group);
   // Kernels after the first start while their predecessor drains (programmatic
   // dependent launch), unless stage boundaries are being timed: an event
   // between two kernels is a full dependency.
@@ -391,6 +393,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g1.a = base + L.a1; g1.a_rows = L.R;
   g1.b = w->w13; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
   g1.offsets = i32(L.expert_offsets); g1.tile_offs = i32(L.tile_offsets); g1.G = Et; g1.N = 2 * I; g1.K = H;
+  g1.tile_group = i32(L.tile_group);
   g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2; g1.gs_q = gs_a2;
   g1.h_dump = h_dump; g1.err = dev_->err; g1.pdl = pdl;
   cudaError_t e = launch_grouped_gemm(g1, s, &why);
@@ -403,6 +406,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g2.a = base + L.a2; g2.a_rows = L.R;
   g2.b = w->w2; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
+  g2.tile_group = i32(L.tile_group);
   g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
   g2.pdl = pdl; g2.early_weights = pdl;  // expert offsets come from the route, two kernels back
   e = launch_grouped_gemm(g2, s, &why);

@@ -127,7 +127,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sche
   }
   x.mt = b / sc.nblocks;
   const int nb = b - x.mt * sc.nblocks;
-  x.g = upper_group(p.tile_offs, p.G, x.mt);
+  x.g = p.tile_group != nullptr ? __ldg(p.tile_group + x.mt) : upper_group(p.tile_offs, p.G, x.mt);
   const int local = x.mt - __ldg(p.tile_offs + x.g);
   x.row0 = __ldg(p.offsets + x.g) + local * BM;
   x.rows = min(BM, __ldg(p.offsets + x.g + 1) - x.row0);
@@ -248,9 +248,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       // L2 prefetch cursor: (tile pf_t, K tile pf_kt), PREFETCH K tiles ahead
       int pf_t = blockIdx.x, pf_kt = 0;
       Tile pf_x{};
-      if (pf_t < total) pf_x = decode_tile(pf_t, p, sc);
       auto prefetch_next = [&]() {
         if (pf_t >= total) return;
+        if (pf_kt == 0) pf_x = decode_tile(pf_t, p, sc);
         const uint8_t* ac = p.a + (static_cast<size_t>(pf_x.mt) * nkt + pf_kt) * TILE_BYTES;
         bulk_prefetch_l2(ac, static_cast<uint32_t>((pf_x.rows + 7) & ~7) * 128u);
         bulk_prefetch_l2(ac + TILE_CODE_BYTES, TILE_SF_BYTES);
@@ -260,10 +260,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         if (++pf_kt == nkt) {
           pf_kt = 0;
           pf_t += gridDim.x;
-          if (pf_t < total) pf_x = decode_tile(pf_t, p, sc);
         }
       };
-      for (int j = 0; j < PREFETCH; ++j) prefetch_next();
+      int pf_ahead = 0;  // prefetches issued; the cursor starts after the first load
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile x = decode_tile(t, p, sc);
         const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
@@ -291,6 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
             bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
           }
+          for (; pf_ahead <= PREFETCH; ++pf_ahead) prefetch_next();
           prefetch_next();
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (ph << stage);

@@ -67,6 +67,7 @@ struct RouteArgs {
   int32_t H;
   const float* gs_a1;       // [E']
   uint8_t* a1;              // TILED_GROUPED operand, K = H
+  int32_t* tile_group;      // nullable [tiles]: expert of each 128-row tile (written with the offsets)
   bool pdl;                 // first kernel as a programmatic dependent launch
 };
 size_t route_scratch_bytes(int32_t T, int32_t E);
@@ -86,6 +87,7 @@ struct GemmArgs {
   const float* gs_b;        // [G]
   const int32_t* offsets;   // [G+1]
   const int32_t* tile_offs; // [G+1]
+  const int32_t* tile_group; // nullable [tile_offs[G]]: group of each 128-row tile of A
   int32_t G, N, K;
   int epilogue;
   void* d;                  // STORE: [rows, ldd]

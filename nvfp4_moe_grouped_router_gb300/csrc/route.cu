@@ -235,6 +235,17 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
       a.offsets[e] = offs[e];
       a.tile_offs[e] = til[e];
     }
+    if (a.tile_group != nullptr) {
+      // expert of every 128-row tile: the last e with til[e] <= tile (searched in shared memory)
+      for (int j = threadIdx.x; j < til[Et]; j += blockDim.x) {
+        int lo = 0, hi = Et;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (til[mid] <= j) lo = mid; else hi = mid;
+        }
+        a.tile_group[j] = lo;
+      }
+    }
   }
   const int t = blockIdx.x * kPermWarps + warp;
   if (t >= T) return;
