@@ -26,9 +26,10 @@
 //               barrier), then the A codes (valid-row prefix) and the B codes,
 //               moved with 1-D bulk copies into a 3-deep ring.
 //               Shared memory holds only three stages, fewer than it takes to
-//               cover the memory latency at full bandwidth, so a second cursor
-//               runs PREFETCH K tiles ahead and asks L2 for the same bytes:
-//               the ring's loads then mostly hit L2.
+//               cover the memory latency at full bandwidth, so the producer
+//               also asks L2 for the weights 4-8 K tiles ahead (one bulk
+//               prefetch per 4 contiguous chunks): the ring's loads then
+//               mostly hit L2.
 //   warp 1      MMA issuer: per K tile the tcgen05.cp copies of the replicated
 //               scales into the stage's TMEM scale slot, then four
 //               128x256x64 MMAs into the single 256-column TMEM accumulator.
@@ -61,7 +62,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int STAGES = 3;
-constexpr int PREFETCH = 4;               // K tiles the L2 prefetch runs ahead of the ring
+constexpr int PF_GROUP = 4;               // K chunks per L2 prefetch instruction
+constexpr int PF_AHEAD = 4;               // K tiles the L2 prefetch stays ahead of the ring
 constexpr int EPI_WARPS = 8;
 constexpr int EXP_WARPS = 2;
 constexpr int THREADS = 64 + 32 * EXP_WARPS + 32 * EPI_WARPS;
@@ -82,7 +84,12 @@ constexpr int REP_BYTES = 6 * REP_BLOCK;
 constexpr int REP_SLOTS = 2;
 
 constexpr int OFF_REP = STAGES * STAGE_BYTES;
-constexpr int OFF_BAR = OFF_REP + REP_SLOTS * REP_BYTES;
+// Group tables copied to shared memory once per CTA (when G + 1 fits), so that
+// decoding a tile costs a binary search in shared memory instead of a chain of
+// dependent global loads on the producer's path.
+constexpr int SMEM_GROUPS = 1025;
+constexpr int OFF_GRP = OFF_REP + REP_SLOTS * REP_BYTES;   // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
+constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
 constexpr int NUM_BARS = 3 * STAGES + REP_SLOTS + 3;  // full, empty, sf_full, rep_full, acc_full/empty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -117,7 +124,13 @@ __device__ __forceinline__ Sched make_sched(const GemmArgs& p) {
   return s;
 }
 
-__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sched& sc) {
+// Group tables for decode_tile: shared-memory copies when present, else global.
+struct Groups {
+  const int* toff;   // [G + 1] in shared memory, or nullptr
+  const int* off;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sched& sc, const Groups& gr = Groups{}) {
   Tile x;
   int b = t, half = -1;
   if (t >= sc.first_split) {
@@ -127,10 +140,21 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sche
   }
   x.mt = b / sc.nblocks;
   const int nb = b - x.mt * sc.nblocks;
-  x.g = p.tile_group != nullptr ? __ldg(p.tile_group + x.mt) : upper_group(p.tile_offs, p.G, x.mt);
-  const int local = x.mt - __ldg(p.tile_offs + x.g);
-  x.row0 = __ldg(p.offsets + x.g) + local * BM;
-  x.rows = min(BM, __ldg(p.offsets + x.g + 1) - x.row0);
+  if (gr.toff != nullptr) {
+    int lo = 0, hi = p.G;  // last g with toff[g] <= mt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (gr.toff[mid] <= x.mt) lo = mid; else hi = mid;
+    }
+    x.g = lo;
+    x.row0 = gr.off[lo] + (x.mt - gr.toff[lo]) * BM;
+    x.rows = min(BM, gr.off[lo + 1] - x.row0);
+  } else {
+    x.g = p.tile_group != nullptr ? __ldg(p.tile_group + x.mt) : upper_group(p.tile_offs, p.G, x.mt);
+    const int local = x.mt - __ldg(p.tile_offs + x.g);
+    x.row0 = __ldg(p.offsets + x.g) + local * BM;
+    x.rows = min(BM, __ldg(p.offsets + x.g + 1) - x.row0);
+  }
   x.wide = half < 0 && (nb + 1) * BN <= p.N;
   x.nt0 = 2 * nb + (half > 0 ? 1 : 0);
   return x;
@@ -219,22 +243,28 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const int nkt = (k64 + 3) >> 2;
   if (p.early_weights && threadIdx.x == 0) {
     // The previous kernel (which produces A) may still be running: start pulling
-    // this CTA's first weight chunks into L2 meanwhile.
+    // this CTA's first weight tile into L2 meanwhile.
     const Sched sc0 = make_sched(p);
-    int t = blockIdx.x, kt = 0;
-    for (int j = 0; j < STAGES + PREFETCH && t < sc0.total; ++j) {
-      const Tile x = decode_tile(t, p, sc0);
-      const uint8_t* bc = p.b + ((static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt + kt) * TILE_BYTES;
-      bulk_prefetch_l2(bc, TILE_BYTES);
-      if (x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, TILE_BYTES);
-      if (++kt == nkt) {
-        kt = 0;
-        t += gridDim.x;
-      }
+    if (static_cast<int>(blockIdx.x) < sc0.total) {
+      const Tile x = decode_tile(blockIdx.x, p, sc0);
+      const uint8_t* bc = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
+      bulk_prefetch_l2(bc, static_cast<uint32_t>(nkt) * TILE_BYTES);
+      if (x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, static_cast<uint32_t>(nkt) * TILE_BYTES);
     }
   }
   griddep_wait();
   griddep_launch_dependents();
+  Groups gr{};
+  if (p.G + 1 <= SMEM_GROUPS) {
+    int* st = reinterpret_cast<int*>(smem + OFF_GRP);
+    for (int j = threadIdx.x; j <= p.G; j += blockDim.x) {
+      st[j] = __ldg(p.tile_offs + j);
+      st[SMEM_GROUPS + j] = __ldg(p.offsets + j);
+    }
+    __syncthreads();
+    gr.toff = st;
+    gr.off = st + SMEM_GROUPS;
+  }
   const Sched sc = make_sched(p);
   const int total = sc.total;
 
@@ -245,26 +275,29 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       uint32_t ph = 0;
       uint32_t pending = 0, pend_par = 0;  // per stage: load issued, parity of that phase
       bool ok = true;
-      // L2 prefetch cursor: (tile pf_t, K tile pf_kt), PREFETCH K tiles ahead
-      int pf_t = blockIdx.x, pf_kt = 0;
+      // L2 prefetch cursor (tile pf_t, K tile pf_kt): weights only (A was just
+      // written by the previous kernel and is in L2), up to PF_GROUP K chunks of
+      // a weight tile per instruction (they are contiguous), kept at least
+      // PF_AHEAD K tiles ahead of the ring's loads.  Every bulk instruction
+      // costs the issuing thread ~100+ cycles, hence the grouping.
+      int pf_t = blockIdx.x, pf_kt = 0, pf_issued = 0, loaded = 0;
       Tile pf_x{};
-      auto prefetch_next = [&]() {
-        if (pf_t >= total) return;
-        if (pf_kt == 0) pf_x = decode_tile(pf_t, p, sc);
-        const uint8_t* ac = p.a + (static_cast<size_t>(pf_x.mt) * nkt + pf_kt) * TILE_BYTES;
-        bulk_prefetch_l2(ac, static_cast<uint32_t>((pf_x.rows + 7) & ~7) * 128u);
-        bulk_prefetch_l2(ac + TILE_CODE_BYTES, TILE_SF_BYTES);
+      auto prefetch_group = [&]() -> bool {
+        if (pf_t >= total) return false;
+        if (pf_kt == 0) pf_x = decode_tile(pf_t, p, sc, gr);
+        const int n = min(PF_GROUP, nkt - pf_kt);
         const uint8_t* bc = p.b + ((static_cast<size_t>(pf_x.g) * ntiles + pf_x.nt0) * nkt + pf_kt) * TILE_BYTES;
-        bulk_prefetch_l2(bc, TILE_BYTES);
-        if (pf_x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, TILE_BYTES);
-        if (++pf_kt == nkt) {
+        bulk_prefetch_l2(bc, static_cast<uint32_t>(n) * TILE_BYTES);
+        if (pf_x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, static_cast<uint32_t>(n) * TILE_BYTES);
+        pf_issued += n;
+        if ((pf_kt += n) == nkt) {
           pf_kt = 0;
           pf_t += gridDim.x;
         }
+        return true;
       };
-      int pf_ahead = 0;  // prefetches issued; the cursor starts after the first load
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile x = decode_tile(t, p, sc);
+        const Tile x = decode_tile(t, p, sc, gr);
         const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
         const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
         const int nbt = x.wide ? 2 : 1;
@@ -290,8 +323,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
             bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
           }
-          for (; pf_ahead <= PREFETCH; ++pf_ahead) prefetch_next();
-          prefetch_next();
+          ++loaded;
+          while (pf_issued < loaded + PF_AHEAD && prefetch_group()) {
+          }
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
           if (++stage == STAGES) {
@@ -316,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       int tile_i = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
-        const Tile x = decode_tile(t, p, sc);
+        const Tile x = decode_tile(t, p, sc, gr);
         const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
         // the epilogue has moved the previous tile out of TMEM
         if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) break;
@@ -358,7 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
     int i = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile x = decode_tile(t, p, sc);
+      const Tile x = decode_tile(t, p, sc, gr);
       for (int kt = 0; kt < nkt; ++kt, ++i) {
         const int s = i % STAGES;
         const int r = i % REP_SLOTS;
@@ -409,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
     const int r = q * 32 + lane;            // tile row handled by this thread
     int tile_i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
-      const Tile x = decode_tile(t, p, sc);
+      const Tile x = decode_tile(t, p, sc, gr);
       if (!mbar_wait(accf_bar, tile_i & 1, abort_flag, p.err, DEV_TIMEOUT_EPILOGUE, t)) break;
       tc_fence_after();
       const bool active = q * 32 < x.rows && (half == 0 || x.wide);
