@@ -352,9 +352,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
         const Tile x = decode_tile(t, p, sc, gr);
         const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
-        // the epilogue has moved the previous tile out of TMEM
-        if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) break;
-        tc_fence_after();
         for (int kt = 0; kt < nkt; ++kt, ++i) {
           const int s = i % STAGES;
           const int r = i % REP_SLOTS;
@@ -373,6 +370,16 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           tc_copy_128x256b(sf, rs + REP_A);
           tc_copy_128x256b(sf + 8, rs + REP_A + REP_BLOCK);
           for (int c = 0; c < (x.wide ? 4 : 2); ++c) tc_copy_128x256b(sf + 16 + c * 8, rs + REP_B + c * REP_BLOCK);
+          if (kt == 0) {
+            // The first K tile's scale copies go out before this wait (they do
+            // not touch the accumulator columns): the epilogue has moved the
+            // previous tile out of TMEM.
+            if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           for (int kk = 0; kk < na; ++kk) {
             const uint32_t sfa = sf + (kk >> 1) * 8 + (kk & 1) * 4;
             const uint32_t sfb = x.wide ? sf + 16 + kk * 8 : sf + 16 + (kk >> 1) * 8 + (kk & 1) * 4;
