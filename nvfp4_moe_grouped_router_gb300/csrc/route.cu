@@ -15,9 +15,10 @@
 //                     so this is exactly the stable order of assignments
 //                     a = t*k + j by expert -- computed in parallel, without
 //                     atomics, deterministically.  With activations given,
-//                     one warp per (token, slot) quantizes the token's row
-//                     with the slot's expert global scale into that slot of
-//                     the gate_up GEMM's TILED_GROUPED operand.
+//                     the token's row is quantized with each slot's expert
+//                     global scale into that slot of the gate_up GEMM's
+//                     TILED_GROUPED operand: one warp per (token, slot) for up
+//                     to 256 tokens, one warp per token above.
 //   combine         : out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ shared row).
 //
 // Sources: top-k routing over many routed experts plus one shared expert
@@ -194,14 +195,38 @@ __device__ __forceinline__ int assignment_pos(const RouteArgs& a, const int* off
   return offs[e] + rank;
 }
 
-// Grid (ceil(T / kPermWarps), slots) with activations (QUANT): warp w of CTA
-// (bx, j) places assignment (t = bx * kPermWarps + w, j) and quantizes token
-// t's row into that slot, one 64-element group per lane.  Without activations
-// the grid is (ceil(T / kPermWarps), 1) and lane j of a warp places slot j.
-template <bool QUANT>
+// Three forms, one warp per token t = bx * kPermWarps + w:
+//   PERM_ONLY  grid (ceil(T / kPermWarps), 1): lane j places slot j.
+//   PERM_SLOT  grid (ceil(T / kPermWarps), slots): CTA (bx, j) places slot j and
+//              quantizes token t's row into it, one 64-element group per lane
+//              (few tokens: spreads the quantization over k times more warps).
+//   PERM_TOKEN grid (ceil(T / kPermWarps), 1): lane j places slot j; then the
+//              warp quantizes the row once per distinct global scale among the
+//              token's slots and stores it to every slot (many tokens: the
+//              arithmetic is done once per token, not once per slot).
+enum PermMode : int { PERM_ONLY = 0, PERM_SLOT = 1, PERM_TOKEN = 2 };
+
+__device__ __forceinline__ void load_group64_bf16(const RouteArgs& a, int t, int gg, float (&v)[64]) {
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                    static_cast<int64_t>(t) * a.H + gg * 64);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 u = __ldg(src + i);
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[i * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
+      v[i * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArgs a, int W) {
   __shared__ int offs[kMaxE + 2];
   __shared__ int til[kMaxE + 2];
+  __shared__ int s_pos[MODE == PERM_TOKEN ? kPermWarps : 1][33];
+  __shared__ int s_exp[MODE == PERM_TOKEN ? kPermWarps : 1][33];
   const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   griddep_wait();
@@ -249,14 +274,41 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
   }
   const int t = blockIdx.x * kPermWarps + warp;
   if (t >= T) return;
-  if constexpr (!QUANT) {
-    if (lane < k + a.shared) {
+  if constexpr (MODE != PERM_SLOT) {
+    const int slots = k + a.shared;
+    if (lane < slots) {
       int e;
       const int pos = assignment_pos(a, offs, W, t, lane, e);
       const int as = lane < k ? t * k + lane : pos;
       a.perm_to_src[pos] = as;
       a.src_to_perm[as] = pos;
       a.perm_token[pos] = t;
+      if constexpr (MODE == PERM_TOKEN) {
+        s_pos[warp][lane] = pos;
+        s_exp[warp][lane] = e;
+      }
+    }
+    if constexpr (MODE == PERM_TOKEN) {
+      __syncwarp();
+      const int gpr = a.H >> 6;
+      for (int gg = lane; gg < gpr; gg += 32) {
+        float v[64];
+        load_group64_bf16(a, t, gg, v);
+        uint32_t w[8];
+        uint32_t sf = 0;
+        float gs_done = -1.0f;  // global scales are positive
+        for (int j = 0; j < slots; ++j) {
+          const int ej = s_exp[warp][j], pj = s_pos[warp][j];
+          const float gs = __ldg(a.gs_a1 + ej);
+          if (gs != gs_done) {
+            sf = quant_group64(v, gs, w);
+            gs_done = gs;
+          }
+          const int local = pj - offs[ej];
+          store_group64(a.a1, nullptr, LAYOUT_TILED_GROUPED, a.H, pj, til[ej] + (local >> 7),
+                        static_cast<uint32_t>(local & 127), gg, w, sf);
+        }
+      }
     }
   } else {
     const int j = blockIdx.y;
@@ -274,18 +326,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
     const int gpr = a.H >> 6;
     for (int gg = lane; gg < gpr; gg += 32) {
       float v[64];
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
-                                                        static_cast<int64_t>(t) * a.H + gg * 64);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 u = __ldg(src + i);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[i * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
-          v[i * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
-        }
-      }
+      load_group64_bf16(a, t, gg, v);
       uint32_t w[8];
       const uint32_t sf = quant_group64(v, gs, w);
       store_group64(a.a1, nullptr, LAYOUT_TILED_GROUPED, a.H, pos, tile, static_cast<uint32_t>(local & 127), gg, w,
@@ -351,13 +392,16 @@ cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
     }
   }
   const int blocks = a.T > 0 ? (a.T + kPermWarps - 1) / kPermWarps : 1;
-  if (a.x != nullptr) {
-    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<true>));
-    e = launch_kernel(route_permute_kernel<true>, dim3(blocks, a.k + a.shared), dim3(kPermWarps * 32), 0, s, pdl, a,
-                      W);
+  if (a.x != nullptr && W <= kInlineWords) {
+    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_SLOT>));
+    e = launch_kernel(route_permute_kernel<PERM_SLOT>, dim3(blocks, a.k + a.shared), dim3(kPermWarps * 32), 0, s,
+                      pdl, a, W);
+  } else if (a.x != nullptr) {
+    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_TOKEN>));
+    e = launch_kernel(route_permute_kernel<PERM_TOKEN>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
   } else {
-    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<false>));
-    e = launch_kernel(route_permute_kernel<false>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
+    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_ONLY>));
+    e = launch_kernel(route_permute_kernel<PERM_ONLY>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
   }
   return e;
 }
