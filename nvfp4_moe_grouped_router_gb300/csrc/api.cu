@@ -290,6 +290,7 @@ nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B
   a.a = A; a.a_rows = a_rows; a.b = B; a.gs_a = gs_a; a.gs_b = gs_b;
   a.offsets = group_offsets; a.tile_offs = tile_offsets; a.G = G; a.N = N; a.K = K;
   a.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
+  a.d_align32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && (ldd * (out_dtype == NVF_F32 ? 4 : 2)) % 32 == 0;
   a.d = D; a.ldd = ldd; a.err = dev_->err;
   const char* why = nullptr;
   cudaError_t e = launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &why);
@@ -408,6 +409,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
   g2.tile_group = i32(L.tile_group);
   g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
+  g2.d_align32 = true;  // 256-byte aligned workspace, H a multiple of 128
   g2.pdl = pdl; g2.early_weights = pdl;  // expert offsets come from the route, two kernels back
   e = launch_grouped_gemm(g2, s, &why);
   if (e != cudaSuccess)

@@ -512,13 +512,25 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           for (int c = 0; c < 4; ++c) {
             const int64_t col = static_cast<int64_t>(nt) * 128 + c * 32;
             if constexpr (EPI == EPI_STORE_F32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.ldd + col);
+              float* drow = static_cast<float*>(p.d) + row * p.ldd + col;
+              if (p.d_align32) {
+                // whole 32-byte sectors per instruction
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__fmul_rn(__uint_as_float(v[c][4 * j]), alpha),
-                                     __fmul_rn(__uint_as_float(v[c][4 * j + 1]), alpha),
-                                     __fmul_rn(__uint_as_float(v[c][4 * j + 2]), alpha),
-                                     __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t o[8];
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][8 * j + e]), alpha));
+                  st_global_v8(drow + 8 * j, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+                }
+              } else {
+                float4* dst = reinterpret_cast<float4*>(drow);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  dst[j] = make_float4(__fmul_rn(__uint_as_float(v[c][4 * j]), alpha),
+                                       __fmul_rn(__uint_as_float(v[c][4 * j + 1]), alpha),
+                                       __fmul_rn(__uint_as_float(v[c][4 * j + 2]), alpha),
+                                       __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
+              }
             } else {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
 #pragma unroll
