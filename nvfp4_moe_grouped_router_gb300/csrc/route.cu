@@ -335,40 +335,55 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
   }
 }
 
+// Eight consecutive outputs of one token per thread: one 256-bit load per slot
+// row (y rows are 32-byte aligned: 256-byte workspace, H % 128 == 0).  The
+// sum runs over the slots in order with one FMA per slot, then the shared row.
+__device__ __forceinline__ void ld_nc_v8(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
 template <int OUT_BF16>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
                                                      void* out) {
   griddep_wait();
-  const int h4 = H >> 2;
-  const int64_t total = static_cast<int64_t>(T) * h4;
+  const int h8 = H >> 3;
+  const int64_t total = static_cast<int64_t>(T) * h8;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(idx / h4);
-    const int c = static_cast<int>(idx - static_cast<int64_t>(t) * h4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t = static_cast<int>(idx / h8);
+    const int c = static_cast<int>(idx - static_cast<int64_t>(t) * h8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       const int64_t a = static_cast<int64_t>(t) * k + j;
       const float wj = __ldg(w + a);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(__ldg(s2p + a)) * H) + c);
-      acc.x = fmaf(wj, v.x, acc.x);
-      acc.y = fmaf(wj, v.y, acc.y);
-      acc.z = fmaf(wj, v.z, acc.z);
-      acc.w = fmaf(wj, v.w, acc.w);
+      float v[8];
+      ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
     }
     if (shared) {
       const int64_t a = static_cast<int64_t>(T) * k + t;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(__ldg(s2p + a)) * H) + c);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      float v[8];
+      ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
     if (OUT_BF16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(t) * H)[c] = u;
+      uint32_t u[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        u[e] = *reinterpret_cast<uint32_t*>(&b);
+      }
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(t) * H)[c] =
+          make_uint4(u[0], u[1], u[2], u[3]);
     } else {
-      reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * H)[c] = acc;
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * H) + 2 * c;
+      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -429,7 +444,7 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
 cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,
                            int32_t shared, int out_dtype, void* out, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  const int64_t total = static_cast<int64_t>(T) * (H / 4);
+  const int64_t total = static_cast<int64_t>(T) * (H / 8);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
