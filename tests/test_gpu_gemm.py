@@ -143,6 +143,23 @@ def test_split_last_round(nvf, out_dtype):
     assert np.all(np.abs(D - ref) <= bound)
 
 
+@pytest.mark.parametrize("rows", [1, 16, 300])
+def test_dense_linear(nvf, rows):
+    """A dense NVFP4 W4A4 linear layer is the grouped GEMM with one group: the
+    pages' second workload (gate_up with K = 5120) at a reduced N."""
+    rng = np.random.default_rng(rows)
+    N, K = 512, 5120
+    a = rng.standard_normal((rows, K)).astype(np.float32)
+    gs_a = np.array([F.global_scale(np.abs(a).max())], np.float32)
+    a_c, a_s = F.quantize_rows(a, gs_a[0])
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w_c, w_s, g = M.quantize_expert_weights(w)
+    gs_w = np.array([g], np.float32)
+    D, offs = _run(nvf, a_c, a_s, [rows], w_c[None], w_s[None], gs_a, gs_w)
+    ref = M.grouped_gemm(a_c, a_s, offs, gs_a, w_c[None], w_s[None], gs_w)
+    assert rel_err(D, ref) <= TOL
+
+
 def test_argument_validation(nvf):
     z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     f = torch.ones(1, dtype=torch.float32, device="cuda")
