@@ -291,6 +291,7 @@ nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B
   a.offsets = group_offsets; a.tile_offs = tile_offsets; a.G = G; a.N = N; a.K = K;
   a.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
   a.d_align32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && (ldd * (out_dtype == NVF_F32 ? 4 : 2)) % 32 == 0;
+  a.small_a = a_rows <= 32;  // no group can hold more rows than the buffer
   a.d = D; a.ldd = ldd; a.err = dev_->err;
   const char* why = nullptr;
   cudaError_t e = launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), &why);
@@ -395,6 +396,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g1.b = w->w13; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
   g1.offsets = i32(L.expert_offsets); g1.tile_offs = i32(L.tile_offsets); g1.G = Et; g1.N = 2 * I; g1.K = H;
   g1.tile_group = i32(L.tile_group);
+  g1.small_a = T <= 32;  // no expert (the shared one included) sees more rows than there are tokens
   g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = base + L.a2; g1.gs_q = gs_a2;
   g1.h_dump = h_dump; g1.err = dev_->err; g1.pdl = pdl;
   cudaError_t e = launch_grouped_gemm(g1, s, &why);
@@ -408,6 +410,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g2.b = w->w2; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
   g2.tile_group = i32(L.tile_group);
+  g2.small_a = T <= 32;
   g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
   g2.d_align32 = true;  // 256-byte aligned workspace, H a multiple of 128
   g2.pdl = pdl; g2.early_weights = pdl;  // expert offsets come from the route, two kernels back

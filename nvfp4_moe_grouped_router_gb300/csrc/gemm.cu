@@ -61,7 +61,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int STAGES = 3;
 constexpr int PF_GROUP = 4;               // K chunks per L2 prefetch instruction
 constexpr int PF_AHEAD = 4;               // K tiles the L2 prefetch stays ahead of the ring
 constexpr int EPI_WARPS = 8;
@@ -71,32 +70,43 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = BN;          // scale slots after the accumulator
 constexpr uint32_t SF_SLOT_COLS = 64;     // A: 16 columns, B: 32 columns
 
-// stage: [A chunk 18432][B codes 2 x 16384][B atoms 2 x 2048]
-constexpr int ST_A = 0;
-constexpr int ST_B = TILE_BYTES;
-constexpr int ST_BSF = ST_B + 2 * TILE_CODE_BYTES;
-constexpr int STAGE_BYTES = ST_BSF + 2 * TILE_SF_BYTES;   // 55296
 // replicated scales per stage: A 2 x 4096 (two K steps each), B 4 x 4096
 constexpr int REP_BLOCK = 4096;
 constexpr int REP_A = 0;
 constexpr int REP_B = 2 * REP_BLOCK;
 constexpr int REP_BYTES = 6 * REP_BLOCK;
 constexpr int REP_SLOTS = 2;
-
-constexpr int OFF_REP = STAGES * STAGE_BYTES;
 // Group tables copied to shared memory once per CTA (when G + 1 fits), so that
 // decoding a tile costs a binary search in shared memory instead of a chain of
 // dependent global loads on the producer's path.
 constexpr int SMEM_GROUPS = 1025;
-constexpr int OFF_GRP = OFF_REP + REP_SLOTS * REP_BYTES;   // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
-constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
-constexpr int NUM_BARS = 3 * STAGES + REP_SLOTS + 3;  // full, empty, sf_full, rep_full, acc_full/empty, drain
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 
-static_assert(SF_COL0 + STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM budget");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0 && REP_BYTES % 1024 == 0, "1024-byte alignment");
+// Shared-memory layout.  A stage is [A codes][A atoms 2048][B codes 2 x 16384]
+// [B atoms 2 x 2048].  When every group has at most 32 rows (a decode batch, a
+// linear layer of a few rows) the A codes need 4 KB instead of 16 KB, and the
+// space buys a fourth stage: a deeper ring is what lets one SM stream weights
+// faster (its pace is the ring's round-trip time, not the bytes per stage).
+// The MMA still reads 128 A rows; in the small layout rows 32..127 fall on the
+// stage's other bytes and give accumulator rows that are never stored.
+template <bool SMALL_A>
+struct Smem {
+  static constexpr int STAGES = SMALL_A ? 4 : 3;
+  static constexpr int A_ROWS = SMALL_A ? 32 : BM;
+  static constexpr int ST_A = 0;
+  static constexpr int ST_ASF = A_ROWS * 128;
+  static constexpr int ST_B = ST_ASF + TILE_SF_BYTES;
+  static constexpr int ST_BSF = ST_B + 2 * TILE_CODE_BYTES;
+  static constexpr int STAGE_BYTES = ST_BSF + 2 * TILE_SF_BYTES;
+  static constexpr int OFF_REP = STAGES * STAGE_BYTES;
+  static constexpr int OFF_GRP = OFF_REP + REP_SLOTS * REP_BYTES;  // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
+  static constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
+  static constexpr int NUM_BARS = 3 * STAGES + REP_SLOTS + 3;  // full, empty, sf_full, rep_full, acc_full/empty, drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(SF_COL0 + STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0 && REP_BYTES % 1024 == 0, "1024-byte alignment");
+};
 
 struct Tile {
   int g, mt, nt0, row0, rows;
@@ -201,8 +211,13 @@ __device__ __forceinline__ void expand_block(uint8_t* dst, const uint8_t* x, con
   }
 }
 
-template <int EPI>
+template <int EPI, bool SMALL_A>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs p) {
+  using SM = Smem<SMALL_A>;
+  constexpr int STAGES = SM::STAGES;
+  constexpr int ST_A = SM::ST_A, ST_ASF = SM::ST_ASF, ST_B = SM::ST_B, ST_BSF = SM::ST_BSF;
+  constexpr int STAGE_BYTES = SM::STAGE_BYTES, OFF_REP = SM::OFF_REP, OFF_GRP = SM::OFF_GRP;
+  constexpr int OFF_BAR = SM::OFF_BAR, OFF_MISC = SM::OFF_MISC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_base = smem_addr(smem);
@@ -302,7 +317,12 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
         const int nbt = x.wide ? 2 : 1;
         // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
-        const uint32_t a_code_bytes = static_cast<uint32_t>((x.rows + 7) & ~7) * 128u;
+        int a_rows = x.rows;
+        if (a_rows > SM::A_ROWS) {  // the caller promised at most 32 rows per group
+          report_error(p.err, DEV_BAD_OFFSETS, t);
+          a_rows = SM::A_ROWS;
+        }
+        const uint32_t a_code_bytes = static_cast<uint32_t>((a_rows + 7) & ~7) * 128u;
         for (int kt = 0; kt < nkt; ++kt) {
           if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
             ok = false;
@@ -312,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
           // scale atoms first: the expanders start on them while the codes arrive
           mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
-          bulk_load(st + ST_A + TILE_CODE_BYTES, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
+          bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
           for (int h = 0; h < nbt; ++h) {
             const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
             bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
@@ -416,7 +436,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         }
         uint8_t* st = smem + s * STAGE_BYTES;
         uint8_t* rep = smem + OFF_REP + r * REP_BYTES;
-        const uint8_t* a_sf = st + ST_A + TILE_CODE_BYTES;
+        const uint8_t* a_sf = st + ST_ASF;
         const uint8_t* b_sf = st + ST_BSF;
         if (x.wide) {
           // A: K steps (0,1) and (2,3); B, 256 rows: per K step, weight tile 0's
@@ -557,13 +577,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <int EPI>
-cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
-  auto k = grouped_gemm_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+template <int EPI, bool SMALL_A>
+cudaError_t launch_layout(const GemmArgs& a, int grid, cudaStream_t s) {
+  auto k = grouped_gemm_kernel<EPI, SMALL_A>;
+  constexpr int bytes = Smem<SMALL_A>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prefer_max_shared(reinterpret_cast<const void*>(k));
-  return launch_kernel(k, dim3(grid), dim3(THREADS), SMEM_BYTES, s, a.pdl, a);
+  return launch_kernel(k, dim3(grid), dim3(THREADS), bytes, s, a.pdl, a);
+}
+
+template <int EPI>
+cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
+  return a.small_a ? launch_layout<EPI, true>(a, grid, s) : launch_layout<EPI, false>(a, grid, s);
 }
 
 }  // namespace

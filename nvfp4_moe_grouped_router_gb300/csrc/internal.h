@@ -97,6 +97,7 @@ struct GemmArgs {
   float* h_dump;            // SWIGLU: nullable [a_rows, N/2]
   int* err;                 // device error word
   bool d_align32;           // STORE: d and ldd * element size are multiples of 32 bytes (256-bit stores)
+  bool small_a;             // every group has at most 32 rows (a deeper pipeline fits)
   int max_ctas;             // 0: one CTA per SM
   bool pdl;                 // programmatic dependent launch
   // offsets / tile_offs were complete before the preceding kernel began, so the
