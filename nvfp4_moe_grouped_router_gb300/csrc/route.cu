@@ -1,5 +1,7 @@
 // Routing, permutation and combine kernels.
 //
+//   route_topk      : (up to 256 tokens) one warp per token, four per CTA:
+//                     top-k and routing weights only.
 //   route_topk_bits : one warp per token: top-k of (logit + bias) by repeated
 //                     warp argmax (ties to the lower expert id) and a softmax
 //                     over the k selected (renormalised) or over all E.  Each
@@ -8,17 +10,19 @@
 //                     32*blockIdx + i chose e.
 //   route_prefix    : (many tokens only) per expert, exclusive prefix of the
 //                     popcounts of its words: how many earlier tokens chose it.
-//   route_permute   : every CTA scans the per-expert counts (expert offsets and
-//                     the 128-row tile prefix); then one warp per token places
-//                     each of its assignments at offsets[e] + (number of earlier
+//   route_small_permute / route_permute : every CTA scans the per-expert
+//                     counts (expert offsets and the 128-row tile prefix);
+//                     each assignment goes to offsets[e] + (number of earlier
 //                     tokens that chose e).  A token picks k distinct experts,
 //                     so this is exactly the stable order of assignments
-//                     a = t*k + j by expert -- computed in parallel, without
-//                     atomics, deterministically.  With activations given,
-//                     the token's row is quantized with each slot's expert
-//                     global scale into that slot of the gate_up GEMM's
-//                     TILED_GROUPED operand: one warp per (token, slot) for up
-//                     to 256 tokens, one warp per token above.
+//                     a = t*k + j by expert -- computed in parallel,
+//                     deterministically.  Up to 256 tokens the bitmaps are
+//                     rebuilt from the ids in shared memory.  With activations
+//                     given, the token's row is quantized with each slot's
+//                     expert global scale into that slot of the gate_up GEMM's
+//                     TILED_GROUPED operand: one 16-element block per lane up
+//                     to 256 tokens, one warp per token (once per distinct
+//                     scale) above.
 //   combine         : out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ shared row).
 //
 // Sources: top-k routing over many routed experts plus one shared expert
@@ -132,6 +136,17 @@ __global__ void __launch_bounds__(topk_threads<NV>()) route_topk_bits_kernel(Rou
   for (int e = threadIdx.x; e < E; e += blockDim.x) a.words[static_cast<int64_t>(blockIdx.x) * E + e] = s_words[e];
 }
 
+// Up to 256 tokens: one token per warp, four warps per CTA, so the top-k of a
+// decode batch spreads over several SMs; writes ids and weights only (the
+// permutation kernel builds the per-expert bitmaps itself).
+template <int NV>
+__global__ void __launch_bounds__(128) route_topk_kernel(RouteArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (t < a.T) topk_token<NV>(a, t, threadIdx.x & 31);
+}
+
 // One warp per expert: exclusive prefix over word columns of the popcounts.
 __global__ void __launch_bounds__(256) route_prefix_kernel(RouteArgs a, int W) {
   griddep_wait();
@@ -195,16 +210,145 @@ __device__ __forceinline__ int assignment_pos(const RouteArgs& a, const int* off
   return offs[e] + rank;
 }
 
-// Three forms, one warp per token t = bx * kPermWarps + w:
-//   PERM_ONLY  grid (ceil(T / kPermWarps), 1): lane j places slot j.
-//   PERM_SLOT  grid (ceil(T / kPermWarps), slots): CTA (bx, j) places slot j and
-//              quantizes token t's row into it, one 64-element group per lane
-//              (few tokens: spreads the quantization over k times more warps).
-//   PERM_TOKEN grid (ceil(T / kPermWarps), 1): lane j places slot j; then the
-//              warp quantizes the row once per distinct global scale among the
-//              token's slots and stores it to every slot (many tokens: the
-//              arithmetic is done once per token, not once per slot).
-enum PermMode : int { PERM_ONLY = 0, PERM_SLOT = 1, PERM_TOKEN = 2 };
+// Expert offsets, tile offsets and the tile -> expert map, from shared memory.
+__device__ __forceinline__ void write_offsets(const RouteArgs& a, const int* offs, const int* til, int Et) {
+  for (int e = threadIdx.x; e <= Et; e += blockDim.x) {
+    a.offsets[e] = offs[e];
+    a.tile_offs[e] = til[e];
+  }
+  if (a.tile_group != nullptr) {
+    // expert of every 128-row tile: the last e with til[e] <= tile
+    for (int j = threadIdx.x; j < til[Et]; j += blockDim.x) {
+      int lo = 0, hi = Et;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (til[mid] <= j) lo = mid; else hi = mid;
+      }
+      a.tile_group[j] = lo;
+    }
+  }
+}
+
+// Up to 256 tokens (W <= kInlineWords bitmap words per expert).  Every CTA
+// rebuilds the per-expert token bitmaps in shared memory from the ids (at most
+// 8 x E words), scans the counts and ranks each assignment by a popcount.
+//   QUANT: grid (ceil(T * wpt / kPermWarps), slots), wpt = ceil(H / 512) warps
+//          per (token, slot); lane l of warp q quantizes 16-element block
+//          32 q + l of the token's row into the slot.  The row is loaded before
+//          the wait on the top-k kernel (x does not depend on it), and every
+//          lane does one block, so a decode batch's quantization has little
+//          latency to hide.
+//   !QUANT: grid (ceil(T / kPermWarps), 1), lane j of a warp places slot j.
+template <bool QUANT>
+__global__ void __launch_bounds__(kPermWarps * 32) route_small_permute_kernel(RouteArgs a, int W) {
+  extern __shared__ uint32_t s_words[];  // [W][E]
+  __shared__ int offs[kMaxE + 2];
+  __shared__ int til[kMaxE + 2];
+  const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wpt = QUANT ? (a.H + 511) / 512 : 1;
+  const int gw = blockIdx.x * kPermWarps + warp;
+  const int t = gw / wpt, q = gw - t * wpt;
+  const int blk = q * 32 + lane;  // 16-element block of the row
+  const bool has_blk = QUANT && t < T && blk < (a.H >> 4);
+  float v[16];
+  if (has_blk) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                      static_cast<int64_t>(t) * a.H + blk * 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 u = __ldg(src + i);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        v[i * 8 + 2 * c] = __uint_as_float(w4[c] << 16);
+        v[i * 8 + 2 * c + 1] = __uint_as_float(w4[c] & 0xFFFF0000u);
+      }
+    }
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) s_words[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int tt = i / k;
+    atomicOr(&s_words[(tt >> 5) * E + __ldg(a.ids + i)], 1u << (tt & 31));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < Et; e += blockDim.x) {
+    int c = T;  // the shared expert sees every token
+    if (e < E) {
+      c = 0;
+      for (int w = 0; w < W; ++w) c += __popc(s_words[w * E + e]);
+    }
+    offs[e] = c;
+    til[e] = (c + 127) >> 7;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int tot = warp_exclusive_scan(offs, Et, lane);
+    const int ttot = warp_exclusive_scan(til, Et, lane);
+    if (lane == 0) {
+      offs[Et] = tot;
+      til[Et] = ttot;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && blockIdx.y == 0) write_offsets(a, offs, til, Et);
+  if (t >= T) return;
+  // position of slot j of token t
+  auto place = [&](int j, int& e) -> int {
+    if (j == k) {
+      e = E;
+      return T * k + t;
+    }
+    e = __ldg(a.ids + static_cast<int64_t>(t) * k + j);
+    const int wc = t >> 5;
+    int rank = __popc(s_words[wc * E + e] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < wc; ++w) rank += __popc(s_words[w * E + e]);
+    return offs[e] + rank;
+  };
+  if constexpr (!QUANT) {
+    if (lane < k + a.shared) {
+      int e;
+      const int pos = place(lane, e);
+      const int as = lane < k ? t * k + lane : pos;
+      a.perm_to_src[pos] = as;
+      a.src_to_perm[as] = pos;
+      a.perm_token[pos] = t;
+    }
+  } else {
+    const int j = blockIdx.y;
+    int e;
+    const int pos = place(j, e);
+    if (q == 0 && lane == 0) {
+      const int as = j < k ? t * k + j : pos;
+      a.perm_to_src[pos] = as;
+      a.src_to_perm[as] = pos;
+      a.perm_token[pos] = t;
+    }
+    if (has_blk) {
+      const float gs = __ldg(a.gs_a1 + e);
+      uint32_t w0, w1;
+      const uint32_t sb = quant_block16(v, gs, __fmul_rn(6.0f, gs), w0, w1);
+      const int local = pos - offs[e];
+      const uint32_t r = static_cast<uint32_t>(local & 127);
+      const int bk = blk & 15;
+      uint8_t* chunk = a.a1 + (static_cast<size_t>(til[e] + (local >> 7)) * num_k_tiles(a.H) + (blk >> 4)) *
+                                  TILE_BYTES;
+      *reinterpret_cast<uint2*>(chunk + tiled_code_offset(r, bk * 8)) = make_uint2(w0, w1);
+      chunk[TILE_CODE_BYTES + (bk >> 2) * 512 + sf_atom_offset(r, bk & 3)] = static_cast<uint8_t>(sb);
+    }
+  }
+}
+
+// More than 256 tokens (bitmaps from route_topk_bits_kernel, ranks from
+// route_prefix_kernel; also the empty batch).  Grid (ceil(T / kPermWarps), 1),
+// one warp per token t = bx * kPermWarps + w; lane j places slot j.  With
+// PERM_TOKEN the warp then quantizes the row once per distinct global scale
+// among the token's slots and stores it to every slot (the arithmetic is done
+// once per token, not once per slot).
+enum PermMode : int { PERM_ONLY = 0, PERM_TOKEN = 2 };
 
 __device__ __forceinline__ void load_group64_bf16(const RouteArgs& a, int t, int gg, float (&v)[64]) {
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
@@ -255,26 +399,10 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
     }
   }
   __syncthreads();
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
-    for (int e = threadIdx.x; e <= Et; e += blockDim.x) {
-      a.offsets[e] = offs[e];
-      a.tile_offs[e] = til[e];
-    }
-    if (a.tile_group != nullptr) {
-      // expert of every 128-row tile: the last e with til[e] <= tile (searched in shared memory)
-      for (int j = threadIdx.x; j < til[Et]; j += blockDim.x) {
-        int lo = 0, hi = Et;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (til[mid] <= j) lo = mid; else hi = mid;
-        }
-        a.tile_group[j] = lo;
-      }
-    }
-  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) write_offsets(a, offs, til, Et);
   const int t = blockIdx.x * kPermWarps + warp;
   if (t >= T) return;
-  if constexpr (MODE != PERM_SLOT) {
+  {
     const int slots = k + a.shared;
     if (lane < slots) {
       int e;
@@ -309,28 +437,6 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
                         static_cast<uint32_t>(local & 127), gg, w, sf);
         }
       }
-    }
-  } else {
-    const int j = blockIdx.y;
-    int e;
-    const int pos = assignment_pos(a, offs, W, t, j, e);
-    if (lane == 0) {
-      const int as = j < k ? t * k + j : pos;
-      a.perm_to_src[pos] = as;
-      a.src_to_perm[as] = pos;
-      a.perm_token[pos] = t;
-    }
-    const float gs = __ldg(a.gs_a1 + e);
-    const int local = pos - offs[e];
-    const int tile = til[e] + (local >> 7);
-    const int gpr = a.H >> 6;
-    for (int gg = lane; gg < gpr; gg += 32) {
-      float v[64];
-      load_group64_bf16(a, t, gg, v);
-      uint32_t w[8];
-      const uint32_t sf = quant_group64(v, gs, w);
-      store_group64(a.a1, nullptr, LAYOUT_TILED_GROUPED, a.H, pos, tile, static_cast<uint32_t>(local & 127), gg, w,
-                    sf);
     }
   }
 }
@@ -395,6 +501,24 @@ cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
   // programmatically on the kernel before them
   bool pdl = a.pdl;
   cudaError_t e = cudaSuccess;
+  if (W > 0 && W <= kInlineWords) {
+    // up to 256 tokens: spread top-k, bitmaps rebuilt in shared memory
+    auto kt = route_topk_kernel<NV>;
+    prefer_max_shared(reinterpret_cast<const void*>(kt));
+    e = launch_kernel(kt, dim3((a.T + 3) / 4), dim3(128), 0, s, pdl, a);
+    if (e != cudaSuccess) return e;
+    const size_t smem = static_cast<size_t>(W) * a.E * sizeof(uint32_t);
+    if (a.x != nullptr) {
+      const int wpt = (a.H + 511) / 512;
+      auto kp = route_small_permute_kernel<true>;
+      prefer_max_shared(reinterpret_cast<const void*>(kp));
+      return launch_kernel(kp, dim3((a.T * wpt + kPermWarps - 1) / kPermWarps, a.k + a.shared),
+                           dim3(kPermWarps * 32), smem, s, true, a, W);
+    }
+    auto kp = route_small_permute_kernel<false>;
+    prefer_max_shared(reinterpret_cast<const void*>(kp));
+    return launch_kernel(kp, dim3((a.T + kPermWarps - 1) / kPermWarps), dim3(kPermWarps * 32), smem, s, true, a, W);
+  }
   if (W > 0) {
     auto kt = route_topk_bits_kernel<NV>;
     prefer_max_shared(reinterpret_cast<const void*>(kt));
@@ -407,11 +531,7 @@ cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
     }
   }
   const int blocks = a.T > 0 ? (a.T + kPermWarps - 1) / kPermWarps : 1;
-  if (a.x != nullptr && W <= kInlineWords) {
-    prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_SLOT>));
-    e = launch_kernel(route_permute_kernel<PERM_SLOT>, dim3(blocks, a.k + a.shared), dim3(kPermWarps * 32), 0, s,
-                      pdl, a, W);
-  } else if (a.x != nullptr) {
+  if (a.x != nullptr) {
     prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_TOKEN>));
     e = launch_kernel(route_permute_kernel<PERM_TOKEN>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
   } else {
@@ -431,7 +551,7 @@ size_t route_scratch_bytes(int32_t T, int32_t E) {
 int route_kernel_launches(int32_t T, int32_t k) {
   (void)k;
   const int W = (T + 31) / 32;
-  return W == 0 ? 1 : (W > kInlineWords ? 3 : 2);
+  return W == 0 ? 1 : (W > kInlineWords ? 3 : 2);  // top-k (+ prefix) + permute
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
