@@ -45,6 +45,7 @@ namespace {
 constexpr int kMaxE = 1024;          // routed experts
 constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
 constexpr int kPermWarps = 16;       // tokens per permute CTA
+constexpr int kCombineSlots = 10;    // the combine keeps up to this many slots in flight per thread
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -450,7 +451,7 @@ __device__ __forceinline__ void ld_nc_v8(const float* p, float (&v)[8]) {
                : "l"(p));
 }
 
-template <int OUT_BF16>
+template <int OUT_BF16, bool BATCH>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
                                                      void* out) {
@@ -462,13 +463,39 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int t = static_cast<int>(idx / h8);
     const int c = static_cast<int>(idx - static_cast<int64_t>(t) * h8);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int64_t a = static_cast<int64_t>(t) * k + j;
-      const float wj = __ldg(w + a);
-      float v[8];
-      ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+    if (BATCH && k <= kCombineSlots) {
+      // Few tokens (latency-bound): all slot rows and weights first, then all
+      // row loads -- two round trips of memory latency instead of two per slot.
+      // Many tokens keep the plain loop: its lower register count keeps more
+      // threads resident, which a bandwidth-bound pass needs more.
+      int64_t row[kCombineSlots];
+      float wv[kCombineSlots];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+      for (int j = 0; j < kCombineSlots; ++j)
+        if (j < k) {
+          const int64_t a = static_cast<int64_t>(t) * k + j;
+          wv[j] = __ldg(w + a);
+          row[j] = static_cast<int64_t>(__ldg(s2p + a)) * H;
+        }
+      float v[kCombineSlots][8];
+#pragma unroll
+      for (int j = 0; j < kCombineSlots; ++j)
+        if (j < k) ld_nc_v8(y + row[j] + c * 8, v[j]);
+#pragma unroll
+      for (int j = 0; j < kCombineSlots; ++j)
+        if (j < k) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[j], v[j][e], acc[e]);
+        }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int64_t a = static_cast<int64_t>(t) * k + j;
+        const float wj = __ldg(w + a);
+        float v[8];
+        ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+      }
     }
     if (shared) {
       const int64_t a = static_cast<int64_t>(T) * k + t;
@@ -568,9 +595,12 @@ cudaError_t launch_combine(const float* y, int32_t H, const float* weights, cons
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
-  prefer_max_shared(reinterpret_cast<const void*>(out_dtype == X_BF16 ? combine_kernel<1> : combine_kernel<0>));
-  return launch_kernel(out_dtype == X_BF16 ? combine_kernel<1> : combine_kernel<0>, dim3(static_cast<unsigned>(blocks)),
-                       dim3(256), 0, s, pdl, y, H, weights, s2p, T, k, shared, out);
+  const bool batch = T <= 256;
+  auto kern = out_dtype == X_BF16 ? (batch ? combine_kernel<1, true> : combine_kernel<1, false>)
+                                  : (batch ? combine_kernel<0, true> : combine_kernel<0, false>);
+  prefer_max_shared(reinterpret_cast<const void*>(kern));
+  return launch_kernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, pdl, y, H, weights, s2p, T, k,
+                       shared, out);
 }
 
 }  // namespace nvf
