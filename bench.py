@@ -154,6 +154,14 @@ def cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s):
     return n * len(tokens) / dt, f"{n} oracle pass(es) over token 0 of the {cfg.name} batch ({len(ow)} experts)"
 
 
+def workload_config(cfg, world):
+    """The `config` object both arms report for workload `cfg`."""
+    return {"workload": f"{cfg.name}: {cfg.description} (T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E}"
+                        f"{'+1 shared' if cfg.shared else ''} top-{cfg.k})",
+            "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "shared": cfg.shared,
+            "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (weights streamed per step)"}
+
+
 def run_reference(args, cfg):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -182,8 +190,8 @@ def run_reference(args, cfg):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
-                       "sample_tokens": len(tokens)},
+            "config": dict(workload_config(cfg, args.gpus), sample_tokens=len(tokens),
+                           timing="oracle on the host, wall clock, one token per sample"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"token 0 of the {cfg.name} batch through the CPU oracle (S1-S7), one core"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -366,12 +374,9 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales) -> f32", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: {cfg.description} (T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E}"
-                                   f"{'+1 shared' if cfg.shared else ''} top-{cfg.k})",
-                       "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k, "shared": cfg.shared,
-                       "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (weights streamed per step)",
-                       "timing": "CUDA graph of the K steps (programmatic dependent launch between kernels), "
-                                 "CUDA events; stage_ms from a second graph with events at stage boundaries"},
+            "config": dict(workload_config(cfg, world),
+                           timing="CUDA graph of the K steps (programmatic dependent launch between kernels), "
+                                  "CUDA events; stage_ms from a second graph with events at stage boundaries"),
             "stage_ms": stage_ms, "stage_graph_ms_per_step": stage_step_ms,
             "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
             "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
