@@ -154,6 +154,18 @@ def cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s):
     return n * len(tokens) / dt, f"{n} oracle pass(es) over token 0 of the {cfg.name} batch ({len(ow)} experts)"
 
 
+def job_time_and_value(elapsed_ms, T, K, dist, device):
+    """Whole-job timing of K steps of T tokens on every rank: the slowest rank's
+    time (max over ranks) and the tokens all ranks processed per second."""
+    t = torch.tensor([float(elapsed_ms)], device=device)
+    world = 1
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        world = dist.get_world_size()
+    ms = float(t.item())
+    return ms, T * K * world / (ms * 1e-3)
+
+
 def workload_config(cfg, world):
     """The `config` object both arms report for workload `cfg`."""
     return {"workload": f"{cfg.name}: {cfg.description} (T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E}"
@@ -314,11 +326,7 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    t = torch.tensor([elapsed_ms], device="cuda")
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms, value = job_time_and_value(start.elapsed_time(end), cfg.T, K, dist, "cuda")
     code, detail = nvf.device_status()
     if code != 0:
         raise RuntimeError(f"device error word {code} at {detail}")
@@ -346,7 +354,7 @@ def main():
         oh.copy_(out, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
+    _, e2e_value = job_time_and_value(e0.elapsed_time(e1), cfg.T, Ke, dist, "cuda")
 
     # --- roofline of the dominant kernel
     L = nvf.workspace_layout(cfg.T, cfg.E, cfg.H, cfg.I, cfg.k, cfg.shared)
@@ -370,7 +378,6 @@ def main():
                 "traffic": None}
 
     ms_step = elapsed_ms / K
-    value = cfg.T * world / (ms_step * 1e-3)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales) -> f32", "data": "synthetic",
@@ -381,7 +388,7 @@ def main():
             "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
             "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
             "roofline": roof, "clocks": clk, "gpu_launches": kernels_per_step(cfg.T) * K,
-            "e2e": {"value": cfg.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
                     "d2h_bytes_per_step": out.numel() * 4}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
