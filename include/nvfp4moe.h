@@ -96,11 +96,23 @@ const char* nvf_last_error_message(void);
 int32_t nvf_abi_version(void);
 
 /* Synchronises `stream`, then reads and clears the current device's error word.
- * *code = 0 if no kernel reported an error, else the kernel's error code
- * (1..4: a pipeline wait expired in the producer / MMA / epilogue / drain);
- * *detail = the tile or stage it happened at.  Returns NVF_ERR_TIMEOUT when a
- * wait expired, NVF_ERR_CUDA on a CUDA error, else NVF_OK. */
+ * *code = 0 if no kernel reported an error, else the first kernel error code
+ * (1..4: a pipeline wait expired in the producer / MMA / epilogue / drain;
+ * 5: a group larger than the GEMM's layout was promised (it then computes
+ * wrong rows but stays in bounds); 6: the wait of nvf_selftest_bounded_wait);
+ * *detail = the tile or stage it happened at.  Returns NVF_ERR_TIMEOUT for
+ * codes 1-4 and 6, NVF_ERR_DEVICE_CHECK for 5, NVF_ERR_CUDA on a CUDA error,
+ * else NVF_OK. */
 nvf_status nvf_device_status(void* stream, int32_t* code, int32_t* detail);
+
+/* Failure-detection self-test (no counterpart on the pages): launches one CTA
+ * that waits on an mbarrier nothing will ever arrive on, through the same
+ * bounded wait the GEMM pipeline uses, with a limit of `limit_ns` (1 us .. 10 s)
+ * instead of the kernels' 2 s.  The wait gives up, records code 6 in the
+ * device error word and the kernel returns: the context stays usable, and
+ * nvf_device_status then reports NVF_ERR_TIMEOUT with code 6.  Asynchronous on
+ * `stream`. */
+nvf_status nvf_selftest_bounded_wait(uint64_t limit_ns, void* stream);
 
 /* Row order of prepared w13 (host helper).  The fused SiLU-and-mul epilogue
  * needs gate and up rows of the same intermediate index side by side: row r of

@@ -29,6 +29,7 @@ SIGNATURES = {
     "nvf_last_error_message": (ctypes.c_char_p, []),
     "nvf_abi_version": (_I32, []),
     "nvf_device_status": (ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "nvf_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, _P]),
     "nvf_w13_row_map": (ctypes.c_int, [_I32, ctypes.POINTER(_I32)]),
     "nvfp4_tiled_bytes": (_SZ, [_I64, _I32, _I32]),
     "nvfp4_global_scale": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
@@ -107,11 +108,16 @@ def _cuda(t: torch.Tensor, name: str):
 
 
 # ----------------------------------------------------------------------------- small helpers
+def selftest_bounded_wait(limit_ns: int):
+    """Launch the failure-detection self-test (a wait that gives up after limit_ns)."""
+    _check(lib().nvf_selftest_bounded_wait(int(limit_ns), _stream()))
+
+
 def device_status():
     """(code, detail) of the current device's error word (synchronises the stream, then clears it)."""
     code, detail = _I32(0), _I32(0)
     st = lib().nvf_device_status(_stream(), ctypes.byref(code), ctypes.byref(detail))
-    if st not in (0, 5):
+    if st not in (0, 5, 6):   # a device-reported timeout or failed device check: returned as the code
         _check(st)
     return code.value, detail.value
 

@@ -165,7 +165,39 @@ nvf_status nvf_device_status(void* stream, int32_t* code, int32_t* detail) {
   *code = h[0];
   if (detail) *detail = h[1];
   if (h[0] == 0) return NVF_OK;
+  if (h[0] == DEV_BAD_OFFSETS)
+    return fail(NVF_ERR_DEVICE_CHECK, "a group held more rows than the GEMM layout was told (at tile %d)", h[1]);
   return fail(NVF_ERR_TIMEOUT, "a kernel pipeline wait expired (code %d, at %d)", h[0], h[1]);
+}
+
+}  // extern "C"
+
+namespace nvf {
+// One CTA waits on an mbarrier that nothing arrives on, through the pipeline's
+// bounded wait; it must give up after limit_ns and record its code.
+__global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait(smem_addr(&bar), 0, &abort_flag, err, DEV_TIMEOUT_SELFTEST, 0, limit_ns);
+}
+}  // namespace nvf
+
+extern "C" {
+
+nvf_status nvf_selftest_bounded_wait(uint64_t limit_ns, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(limit_ns >= 1000 && limit_ns <= 10000000000ull, "limit_ns=%llu must be in [1e3, 1e10]",
+              static_cast<unsigned long long>(limit_ns));
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_->err, limit_ns);
+  NVF_CUDA(cudaGetLastError(), "self-test launch");
+  return NVF_OK;
 }
 
 nvf_status nvf_w13_row_map(int32_t I, int32_t* map) {

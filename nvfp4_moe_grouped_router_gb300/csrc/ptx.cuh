@@ -23,6 +23,7 @@ enum DeviceError : int {
   DEV_TIMEOUT_EPILOGUE = 3,
   DEV_TIMEOUT_DRAIN = 4,
   DEV_BAD_OFFSETS = 5,
+  DEV_TIMEOUT_SELFTEST = 6,
 };
 
 // A wait that has not completed after this long is a bug: record it and leave.
@@ -78,17 +79,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitTimeoutNs (recording `code` in the error word and raising the CTA's
-// abort flag) or as soon as another role of the CTA has raised the flag.
+// limit_ns (recording `code` in the error word and raising the CTA's abort
+// flag) or as soon as another role of the CTA has raised the flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                          int code, int detail) {
+                                          int code, int detail, uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         report_error(err, code, detail);
         *abort_flag = 1;
         return false;
