@@ -24,12 +24,10 @@
 //   warp 0      producer: per K tile the scale atoms of the A chunk and of the
 //               two B chunks of the tile's 256 weight rows (first, on their own
 //               barrier), then the A codes (valid-row prefix) and the B codes,
-//               moved with 1-D bulk copies into a 3-deep ring.
-//               Shared memory holds only three stages, fewer than it takes to
-//               cover the memory latency at full bandwidth, so the producer
-//               also asks L2 for the weights 4-8 K tiles ahead (one bulk
-//               prefetch per 4 contiguous chunks): the ring's loads then
-//               mostly hit L2.
+//               moved with 1-D bulk copies into a 3-deep ring.  It issues
+//               nothing else: L2 prefetches of the weights further ahead
+//               competed with the ring's own loads and cost the one issuing
+//               thread ~100+ cycles each, and measured slower at every depth.
 //   warp 1      MMA issuer: per K tile the tcgen05.cp copies of the replicated
 //               scales into the stage's TMEM scale slot, then four
 //               128x256x64 MMAs into the single 256-column TMEM accumulator.
@@ -61,8 +59,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int PF_GROUP = 4;               // K chunks per L2 prefetch instruction
-constexpr int PF_AHEAD = 4;               // K tiles the L2 prefetch stays ahead of the ring
 constexpr int EPI_WARPS = 8;
 constexpr int EXP_WARPS = 2;
 constexpr int THREADS = 64 + 32 * EXP_WARPS + 32 * EPI_WARPS;
@@ -290,27 +286,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       uint32_t ph = 0;
       uint32_t pending = 0, pend_par = 0;  // per stage: load issued, parity of that phase
       bool ok = true;
-      // L2 prefetch cursor (tile pf_t, K tile pf_kt): weights only (A was just
-      // written by the previous kernel and is in L2), up to PF_GROUP K chunks of
-      // a weight tile per instruction (they are contiguous), kept at least
-      // PF_AHEAD K tiles ahead of the ring's loads.  Every bulk instruction
-      // costs the issuing thread ~100+ cycles, hence the grouping.
-      int pf_t = blockIdx.x, pf_kt = 0, pf_issued = 0, loaded = 0;
-      Tile pf_x{};
-      auto prefetch_group = [&]() -> bool {
-        if (pf_t >= total) return false;
-        if (pf_kt == 0) pf_x = decode_tile(pf_t, p, sc, gr);
-        const int n = min(PF_GROUP, nkt - pf_kt);
-        const uint8_t* bc = p.b + ((static_cast<size_t>(pf_x.g) * ntiles + pf_x.nt0) * nkt + pf_kt) * TILE_BYTES;
-        bulk_prefetch_l2(bc, static_cast<uint32_t>(n) * TILE_BYTES);
-        if (pf_x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, static_cast<uint32_t>(n) * TILE_BYTES);
-        pf_issued += n;
-        if ((pf_kt += n) == nkt) {
-          pf_kt = 0;
-          pf_t += gridDim.x;
-        }
-        return true;
-      };
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile x = decode_tile(t, p, sc, gr);
         const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
@@ -342,9 +317,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           for (int h = 0; h < nbt; ++h) {
             const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
             bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
-          }
-          ++loaded;
-          while (pf_issued < loaded + PF_AHEAD && prefetch_group()) {
           }
           pending |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
