@@ -12,39 +12,33 @@
 // block is 128 wide when N % 256 == 128); one MMA per 64-element K step is
 // 128 x 256 x 64.  On this part the tensor pipe charges per instruction rather
 // than per FLOP: an MMA costs about the same for N = 16..128 and only a third
-// more at N = 256, and every tcgen05.cp costs about as much as an MMA whatever
-// its shape.  So the kernel uses the widest MMA and moves each operand's scale
-// factors with one 128x256b copy per two K steps (A) or per K step and 256
-// rows (B), instead of one 32x128b.warpx4 copy per K step and 128 rows.  That
-// copy wants the scales already replicated the way the MMA reads them (each
-// 32-lane quarter of TMEM reads its own copy), which two warps build in shared
-// memory from the compact 512-byte atoms of the operand chunks.
+// more at N = 256, and a tcgen05.cp costs about as much as an MMA whatever its
+// shape.  So the kernel uses the widest MMA and keeps the scale factors off the
+// tensor pipe altogether: four warps, one per 32-lane quarter of TMEM, write
+// them with tcgen05.st in the layout the MMA reads (each quarter holds its own
+// copy of B's scales; A row r's scales sit in lane r).
 //
-// Roles (one CTA per SM, persistent, 384 threads):
-//   warp 0      producer: per K tile the scale atoms of the A chunk and of the
+// Roles (one CTA per SM, persistent, 448 threads):
+//   warps 0-3   scale writers: as soon as a stage's scale atoms have landed
+//               (while its codes are still arriving), load them from shared
+//               memory and store them into the stage's TMEM scale slot (warp q
+//               writes lanes 32q..32q+31), then signal sf_ready.
+//   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, 128 columns
+//               each.  They move the accumulator to registers and release it
+//               at once (the next tile's MMAs start), then apply
+//               alpha and store FP32/BF16 rows, or h = silu(gate) * up
+//               requantized to NVFP4 straight into the next GEMM's tiled
+//               operand.
+//   warp 12     producer: per K tile the scale atoms of the A chunk and of the
 //               two B chunks of the tile's 256 weight rows (first, on their own
 //               barrier), then the A codes (valid-row prefix) and the B codes,
-//               moved with 1-D bulk copies into a 3-deep ring.  It issues
+//               moved with 1-D bulk copies into a 4- or 5-deep ring.  It issues
 //               nothing else: L2 prefetches of the weights further ahead
 //               competed with the ring's own loads and cost the one issuing
 //               thread ~100+ cycles each, and measured slower at every depth.
-//   warp 1      MMA issuer: per K tile the tcgen05.cp copies of the replicated
-//               scales into the stage's TMEM scale slot, then four
-//               128x256x64 MMAs into the single 256-column TMEM accumulator.
-//               One thread issues both, so the in-order tensor pipe needs no
-//               barrier between a copy and the MMAs that read it and never
-//               idles while the next K tile's data is ready.
-//   warps 2-3   scale expanders: as soon as a stage's atoms have landed (while
-//               its codes are still arriving), copy them into the replicated
-//               128 x 32-byte layout (core matrices of 8 rows x 16 bytes) of
-//               one of two replica slots, half of the blocks each, and signal
-//               rep_full.
-//   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, 128 columns
-//               each.  They move the accumulator to registers and release it
-//               at once, so the next tile's MMAs start while they compute:
-//               scale by alpha, then store FP32/BF16 rows, or
-//               h = silu(gate) * up requantized to NVFP4 straight into the
-//               next GEMM's tiled operand.
+//   warp 13     MMA issuer: per K tile, once the codes have landed and the
+//               scales are in TMEM, four 128x256x64 MMAs into the single
+//               256-column TMEM accumulator.
 // Every mbarrier wait is bounded; on timeout the kernel records an error word,
 // drains what it issued, frees TMEM and returns.
 #include "internal.h"
@@ -59,19 +53,15 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
+constexpr int SF_WARPS = 4;               // warps 0-3: scale writers, one per TMEM lane quarter
+constexpr int EPI_WARP0 = SF_WARPS;        // warps 4-11: epilogue
 constexpr int EPI_WARPS = 8;
-constexpr int EXP_WARPS = 2;
-constexpr int THREADS = 64 + 32 * EXP_WARPS + 32 * EPI_WARPS;
+constexpr int PRODUCER_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int MMA_WARP = PRODUCER_WARP + 1;
+constexpr int THREADS = 32 * (MMA_WARP + 1);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = BN;          // scale slots after the accumulator
-constexpr uint32_t SF_SLOT_COLS = 64;     // A: 16 columns, B: 32 columns
-
-// replicated scales per stage: A 2 x 4096 (two K steps each), B 4 x 4096
-constexpr int REP_BLOCK = 4096;
-constexpr int REP_A = 0;
-constexpr int REP_B = 2 * REP_BLOCK;
-constexpr int REP_BYTES = 6 * REP_BLOCK;
-constexpr int REP_SLOTS = 2;
+constexpr uint32_t SF_SLOT_COLS = 48;     // A: 16 columns, B: 32 columns
 // Group tables copied to shared memory once per CTA (when G + 1 fits), so that
 // decoding a tile costs a binary search in shared memory instead of a chain of
 // dependent global loads on the producer's path.
@@ -80,28 +70,27 @@ constexpr int SMEM_GROUPS = 1025;
 // Shared-memory layout.  A stage is [A codes][A atoms 2048][B codes 2 x 16384]
 // [B atoms 2 x 2048].  When every group has at most 32 rows (a decode batch, a
 // linear layer of a few rows) the A codes need 4 KB instead of 16 KB, and the
-// space buys a fourth stage: a deeper ring is what lets one SM stream weights
+// space buys a fifth stage: a deeper ring is what lets one SM stream weights
 // faster (its pace is the ring's round-trip time, not the bytes per stage).
 // The MMA still reads 128 A rows; in the small layout rows 32..127 fall on the
 // stage's other bytes and give accumulator rows that are never stored.
 template <bool SMALL_A>
 struct Smem {
-  static constexpr int STAGES = SMALL_A ? 4 : 3;
+  static constexpr int STAGES = SMALL_A ? 5 : 4;
   static constexpr int A_ROWS = SMALL_A ? 32 : BM;
   static constexpr int ST_A = 0;
   static constexpr int ST_ASF = A_ROWS * 128;
   static constexpr int ST_B = ST_ASF + TILE_SF_BYTES;
   static constexpr int ST_BSF = ST_B + 2 * TILE_CODE_BYTES;
   static constexpr int STAGE_BYTES = ST_BSF + 2 * TILE_SF_BYTES;
-  static constexpr int OFF_REP = STAGES * STAGE_BYTES;
-  static constexpr int OFF_GRP = OFF_REP + REP_SLOTS * REP_BYTES;  // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
+  static constexpr int OFF_GRP = STAGES * STAGE_BYTES;  // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
   static constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
-  static constexpr int NUM_BARS = 3 * STAGES + REP_SLOTS + 3;  // full, empty, sf_full, rep_full, acc_full/empty, drain
+  static constexpr int NUM_BARS = 4 * STAGES + 3;  // full, empty, sf_full, sf_ready per stage; acc_full/empty, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(SF_COL0 + STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(BYTES <= 227 * 1024, "shared memory budget");
-  static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0 && REP_BYTES % 1024 == 0, "1024-byte alignment");
+  static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0, "1024-byte alignment");
 };
 
 struct Tile {
@@ -179,31 +168,35 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
-// One 128 x 256-bit TMEM copy: lane l, column c + j receives bytes [4j, 4j+4)
-// of row l of a source stored as core matrices of 8 rows x 16 bytes: row l's
-// first 16 bytes at (l / 8) * 256 + (l % 8) * 16, its second 16 at + 128.
-__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint32_t saddr) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(smem_desc(saddr, 128, 256, kSwizzleNone))
-               : "memory");
+// The scales of one K tile (four 64-element K steps), as the MMA reads them
+// from TMEM.  Scale atom (512 bytes, one per K step and 128 rows): 16 bytes per
+// atom row j, word c holding the four UE4M3 scales of row j + 32 c.  Lane l of
+// every 32-lane quarter receives atom row l:
+//   A (128 rows):      column 4 kk + c    = A atom kk, word c (the MMA reads
+//                      A row r at lane r, column 4 kk + r / 32)
+//   B, 256 rows:       column 16 + 8 kk + c     = weight tile 0's atom kk, word c
+//                      column 16 + 8 kk + 4 + c = weight tile 1's atom kk, word c
+//   B, 128 rows:       column 16 + 4 kk + c     = the weight tile's atom kk, word c
+// (the MMA reads B's scales from each quarter's own copy).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Build one 4 KB replicated block from two 512-byte atoms X, Y: row l of the
-// 128 x 32-byte source = [X row l % 32 | Y row l % 32].  After the copy, lane
-// l holds X's scales of rows l % 32 + 32 c in columns c (c < 4) and Y's in
-// columns 4 + c: every lane quarter sees the same 32 x 8 words, which is how
-// the MMA reads B's scales, and lane r column r / 32 (+ 4) is A row r's.
-// 32 lanes, 64 source units of 16 bytes: two per lane, each stored 4 times.
-__device__ __forceinline__ void expand_block(uint8_t* dst, const uint8_t* x, const uint8_t* y, int lane) {
+// Load atoms `src + kk * 512` (kk < 4), row `lane`, into v[4 kk .. 4 kk + 3].
+__device__ __forceinline__ void load_atom_rows(uint32_t (&v)[16], const uint8_t* src, int lane) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int u = lane + 32 * i;         // 0..63
-    const int h = u >> 5;                // 0: X, 1: Y
-    const int j = (u >> 3) & 3;          // 8-row group within the 32 atom rows
-    const int x16 = u & 7;               // row within the group
-    const uint4 v = *reinterpret_cast<const uint4*>((h ? y : x) + j * 128 + x16 * 16);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<uint4*>(dst + q * 1024 + j * 256 + h * 128 + x16 * 16) = v;
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint4 w = *reinterpret_cast<const uint4*>(src + kk * 512 + lane * 16);
+    v[4 * kk] = w.x;
+    v[4 * kk + 1] = w.y;
+    v[4 * kk + 2] = w.z;
+    v[4 * kk + 3] = w.w;
   }
 }
 
@@ -212,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   using SM = Smem<SMALL_A>;
   constexpr int STAGES = SM::STAGES;
   constexpr int ST_A = SM::ST_A, ST_ASF = SM::ST_ASF, ST_B = SM::ST_B, ST_BSF = SM::ST_BSF;
-  constexpr int STAGE_BYTES = SM::STAGE_BYTES, OFF_REP = SM::OFF_REP, OFF_GRP = SM::OFF_GRP;
+  constexpr int STAGE_BYTES = SM::STAGE_BYTES, OFF_GRP = SM::OFF_GRP;
   constexpr int OFF_BAR = SM::OFF_BAR, OFF_MISC = SM::OFF_MISC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,8 +214,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto repfull_bar = [&](int r) { return bar0 + 8u * (3 * STAGES + r); };
-  const uint32_t accf_bar = bar0 + 8u * (3 * STAGES + REP_SLOTS);
+  auto sfready_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };
+  const uint32_t accf_bar = bar0 + 8u * (4 * STAGES);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_mma_bar = accf_bar + 16u;
   auto stage_addr = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
@@ -235,15 +228,15 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sffull_bar(s), 1);
+      mbar_init(sfready_bar(s), SF_WARPS);
     }
-    for (int r = 0; r < REP_SLOTS; ++r) mbar_init(repfull_bar(r), EXP_WARPS);
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, EPI_WARPS);
     mbar_init(drain_mma_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
+  if (warp == MMA_WARP) tmem_alloc(smem_addr(tmem_holder), TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -279,7 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const Sched sc = make_sched(p);
   const int total = sc.total;
 
-  if (warp == 0) {
+  if (warp == PRODUCER_WARP) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int stage = 0;
@@ -335,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       int i = 0;  // K tiles consumed so far (ring position)
@@ -346,35 +339,27 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
         for (int kt = 0; kt < nkt; ++kt, ++i) {
           const int s = i % STAGES;
-          const int r = i % REP_SLOTS;
-          // Stage landed and its scales are expanded.  TMEM slot s was last read by
-          // the MMAs of K tile i - 3, complete since the producer refilled stage s.
+          // Stage landed and its scales are in TMEM slot s (written after the
+          // MMAs of K tile i - STAGES, which last read the slot, completed).
           if (!mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t) ||
-              !mbar_wait(repfull_bar(r), (i / REP_SLOTS) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+              !mbar_wait(sfready_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
             ok = false;
             break;
+          }
+          if (kt == 0) {
+            // the epilogue has moved the previous tile out of TMEM
+            if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
           const int na = min(4, k64 - kt * 4);
           const uint32_t st = stage_addr(s);
           const uint32_t sf = tmem + SF_COL0 + s * SF_SLOT_COLS;
-          const uint32_t rs = s_base + static_cast<uint32_t>(OFF_REP + r * REP_BYTES);
-          tc_copy_128x256b(sf, rs + REP_A);
-          tc_copy_128x256b(sf + 8, rs + REP_A + REP_BLOCK);
-          for (int c = 0; c < (x.wide ? 4 : 2); ++c) tc_copy_128x256b(sf + 16 + c * 8, rs + REP_B + c * REP_BLOCK);
-          if (kt == 0) {
-            // The first K tile's scale copies go out before this wait (they do
-            // not touch the accumulator columns): the epilogue has moved the
-            // previous tile out of TMEM.
-            if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
           for (int kk = 0; kk < na; ++kk) {
-            const uint32_t sfa = sf + (kk >> 1) * 8 + (kk & 1) * 4;
-            const uint32_t sfb = x.wide ? sf + 16 + kk * 8 : sf + 16 + (kk >> 1) * 8 + (kk & 1) * 4;
+            const uint32_t sfa = sf + kk * 4;
+            const uint32_t sfb = sf + 16 + (x.wide ? kk * 8 : kk * 4);
             tc_mma_nvfp4(tmem, operand_desc_sw128(st + ST_A + kk * 32), operand_desc_sw128(st + ST_B + kk * 32),
                          idesc, sfa, sfb, (kt | kk) != 0 ? 1u : 0u);
           }
@@ -386,98 +371,99 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       tc_commit(drain_mma_bar);
       mbar_wait_drain(drain_mma_bar, 0, p.err, -1);
     }
-  } else if (warp < 2 + EXP_WARPS) {
-    // -------------------------------------------------------------- scale expander
+  } else if (warp < SF_WARPS) {
+    // -------------------------------------------------------------- scale writers
+    const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lane quarter
     int i = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile x = decode_tile(t, p, sc, gr);
       for (int kt = 0; kt < nkt; ++kt, ++i) {
         const int s = i % STAGES;
-        const int r = i % REP_SLOTS;
-        // The stage's atoms landed; the copies that last read replica slot r (K tile i - 2) are
-        // done (its MMAs and copies have completed).  Every lane waits (and
-        // acquires); the warp leaves together if any lane gave up.
-        bool got = mbar_wait(sffull_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
-        if (got && i >= REP_SLOTS)
-          got = mbar_wait(empty_bar((i - REP_SLOTS) % STAGES), ((i - REP_SLOTS) / STAGES) & 1, abort_flag, p.err,
-                          DEV_TIMEOUT_PRODUCER, t);
+        // The stage's atoms landed.  The MMAs of K tile i - STAGES, the last to
+        // read TMEM slot s, completed before the producer refilled the stage.
+        // Every lane waits (and acquires); the warp leaves together if any lane gave up.
+        const bool got = mbar_wait(sffull_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * STAGE_BYTES;
-        uint8_t* rep = smem + OFF_REP + r * REP_BYTES;
-        const uint8_t* a_sf = st + ST_ASF;
-        const uint8_t* b_sf = st + ST_BSF;
+        tc_fence_after();
+        const uint8_t* st = smem + s * STAGE_BYTES;
+        const uint32_t col = tmem + lanes + SF_COL0 + s * SF_SLOT_COLS;
+        uint32_t v[16];
+        load_atom_rows(v, st + ST_ASF, lane);
+        tmem_st16(col, v);
         if (x.wide) {
-          // A: K steps (0,1) and (2,3); B, 256 rows: per K step, weight tile 0's
-          // atom and weight tile 1's.  Expander 0 takes A and B step 0.
-          if (warp == 2) {
-            expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
-            expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
-            expand_block(rep + REP_B, b_sf, b_sf + TILE_SF_BYTES, lane);
-          } else {
+          // 8 columns per K step: tile 0's atom row, then tile 1's
+          uint32_t w[16];
+          load_atom_rows(v, st + ST_BSF, lane);
+          load_atom_rows(w, st + ST_BSF + TILE_SF_BYTES, lane);
+          uint32_t lo[16], hi[16];
 #pragma unroll
-            for (int kk = 1; kk < 4; ++kk)
-              expand_block(rep + REP_B + kk * REP_BLOCK, b_sf + kk * 512, b_sf + TILE_SF_BYTES + kk * 512, lane);
-          }
-        } else if (warp == 2) {
-          expand_block(rep + REP_A, a_sf, a_sf + 512, lane);
-          expand_block(rep + REP_A + REP_BLOCK, a_sf + 1024, a_sf + 1536, lane);
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              lo[8 * kk + c] = v[4 * kk + c];
+              lo[8 * kk + 4 + c] = w[4 * kk + c];
+              hi[8 * kk + c] = v[4 * (kk + 2) + c];
+              hi[8 * kk + 4 + c] = w[4 * (kk + 2) + c];
+            }
+          tmem_st16(col + 16, lo);
+          tmem_st16(col + 32, hi);
         } else {
-          expand_block(rep + REP_B, b_sf, b_sf + 512, lane);
-          expand_block(rep + REP_B + REP_BLOCK, b_sf + 1024, b_sf + 1536, lane);
+          load_atom_rows(v, st + ST_BSF, lane);
+          tmem_st16(col + 16, v);
         }
-        // make the generic-proxy stores visible to the copies (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(repfull_bar(r));
+        if (lane == 0) mbar_arrive(sfready_bar(s));
       }
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2 - EXP_WARPS) >> 2;  // which 128 of the tile's 256 columns
+    const int half = (warp - EPI_WARP0) >> 2;  // which 128 of the tile's 256 columns
     const int r = q * 32 + lane;            // tile row handled by this thread
     int tile_i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
       const Tile x = decode_tile(t, p, sc, gr);
+      const bool active = q * 32 < x.rows && (half == 0 || x.wide);
+      // per-tile constants, fetched while the tile's MMAs run
+      const float alpha = active ? __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g)) : 0.0f;
+      float gsq = 0.0f;
+      if constexpr (EPI == EPI_SWIGLU_QUANT) gsq = active ? __ldg(p.gs_q + x.g) : 0.0f;
       if (!mbar_wait(accf_bar, tile_i & 1, abort_flag, p.err, DEV_TIMEOUT_EPILOGUE, t)) break;
       tc_fence_after();
-      const bool active = q * 32 < x.rows && (half == 0 || x.wide);
-      uint32_t v[4][32];
-      if (active) {
-        const uint32_t tb = tmem + half * 128 + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tb + c * 32, v[c]);
-        tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar);  // accumulator is in registers: release it
-      if (!active) continue;
-      const float alpha = __fmul_rn(__ldg(p.gs_a + x.g), __ldg(p.gs_b + x.g));
+      const uint32_t tb = tmem + half * 128 + (static_cast<uint32_t>(q * 32) << 16);
       const bool valid = r < x.rows;
       const int64_t row = static_cast<int64_t>(x.row0) + r;
       const int nt = x.nt0 + half;          // 128-column weight tile of this warp
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar);  // accumulator is in registers: release it
+      };
       if constexpr (EPI == EPI_SWIGLU_QUANT) {
         // Prepared w13 rows: in every 32-column chunk c of weight tile nt, the
         // first 16 columns are gate rows and the last 16 the matching up rows
-        // of intermediate indices nt * 64 + 16 c .. + 15.
+        // of intermediate indices nt * 64 + 16 c .. + 15.  Chunks 0-2 are
+        // loaded, chunk 0 is turned into its NVFP4 block, chunk 3 is loaded in
+        // its place and the accumulator released: at most 96 accumulator
+        // values are live at once.
         const int I = p.N >> 1;
-        const float gsq = __ldg(p.gs_q + x.g);
         const float six_gsq = __fmul_rn(6.0f, gsq);
+        uint32_t v[3][32];
         uint32_t cw[8];
         uint32_t sfw = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        auto block = [&](const uint32_t (&a)[32], int c) {
           float h[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             // rows past the group's end carry whatever their scale bytes held: use zeros
-            const float g = valid ? __fmul_rn(__uint_as_float(v[c][j]), alpha) : 0.0f;
-            const float u = valid ? __fmul_rn(__uint_as_float(v[c][16 + j]), alpha) : 0.0f;
+            const float g = valid ? __fmul_rn(__uint_as_float(a[j]), alpha) : 0.0f;
+            const float u = valid ? __fmul_rn(__uint_as_float(a[16 + j]), alpha) : 0.0f;
             h[j] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
           }
           if (p.h_dump != nullptr && valid) {
@@ -486,7 +472,20 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
           }
           sfw |= quant_block16(h, gsq, six_gsq, cw[2 * c], cw[2 * c + 1]) << (8 * c);
+        };
+        if (active) {
+#pragma unroll
+          for (int c = 0; c < 3; ++c) tmem_ld32(tb + c * 32, v[c]);
+          tmem_ld_wait();
+          block(v[0], 0);
+          tmem_ld32(tb + 96, v[0]);
+          tmem_ld_wait();
         }
+        release();
+        if (!active) continue;
+        block(v[1], 1);
+        block(v[2], 2);
+        block(v[0], 3);
         // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): weight tile
         // nt's 64 h values are MMA step nt % 4 of K tile nt / 4: 32 code bytes
         // and 4 scale bytes of row r.
@@ -499,10 +498,21 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         }
         *reinterpret_cast<uint32_t*>(chunk + TILE_CODE_BYTES + (nt & 3) * 512 + sf_atom_offset(r, 0)) = sfw;
       } else {
-        if (valid) {
+        // Two passes of 64 columns: the first pass's stores go out before the
+        // second pass's loads, so only 64 accumulator values are ever live.
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int64_t col = static_cast<int64_t>(nt) * 128 + c * 32;
+        for (int pass = 0; pass < 2; ++pass) {
+          uint32_t v[2][32];
+          if (active) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tmem_ld32(tb + pass * 64 + c * 32, v[c]);
+            tmem_ld_wait();
+          }
+          if (pass == 1) release();
+          if (!active || !valid) continue;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int64_t col = static_cast<int64_t>(nt) * 128 + pass * 64 + c * 32;
             if constexpr (EPI == EPI_STORE_F32) {
               float* drow = static_cast<float*>(p.d) + row * p.ldd + col;
               if (p.d_align32) {
@@ -546,7 +556,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 template <int EPI, bool SMALL_A>
