@@ -448,13 +448,13 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       if constexpr (EPI == EPI_SWIGLU_QUANT) {
         // Prepared w13 rows: in every 32-column chunk c of weight tile nt, the
         // first 16 columns are gate rows and the last 16 the matching up rows
-        // of intermediate indices nt * 64 + 16 c .. + 15.  Chunks 0-2 are
-        // loaded, chunk 0 is turned into its NVFP4 block, chunk 3 is loaded in
-        // its place and the accumulator released: at most 96 accumulator
-        // values are live at once.
+        // of intermediate indices nt * 64 + 16 c .. + 15.  Chunks 0-1 are
+        // loaded; each quantized chunk's registers take the next chunk, and the
+        // accumulator is released once chunk 3 is in: at most 64 accumulator
+        // values are live, so nothing spills to (L2-backed) local memory.
         const int I = p.N >> 1;
         const float six_gsq = __fmul_rn(6.0f, gsq);
-        uint32_t v[3][32];
+        uint32_t v[2][32];
         uint32_t cw[8];
         uint32_t sfw = 0;
         auto block = [&](const uint32_t (&a)[32], int c) {
@@ -475,17 +475,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         };
         if (active) {
 #pragma unroll
-          for (int c = 0; c < 3; ++c) tmem_ld32(tb + c * 32, v[c]);
+          for (int c = 0; c < 2; ++c) tmem_ld32(tb + c * 32, v[c]);
           tmem_ld_wait();
           block(v[0], 0);
-          tmem_ld32(tb + 96, v[0]);
+          tmem_ld32(tb + 64, v[0]);
+          tmem_ld_wait();
+          block(v[1], 1);
+          tmem_ld32(tb + 96, v[1]);
           tmem_ld_wait();
         }
         release();
         if (!active) continue;
-        block(v[1], 1);
-        block(v[2], 2);
-        block(v[0], 3);
+        block(v[0], 2);
+        block(v[1], 3);
         // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): weight tile
         // nt's 64 h values are MMA step nt % 4 of K tile nt / 4: 32 code bytes
         // and 4 scale bytes of row r.

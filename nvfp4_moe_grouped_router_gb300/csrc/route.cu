@@ -36,6 +36,7 @@
 #include "layout.cuh"
 #include "ptx.cuh"
 #include "quant_block.cuh"
+#include "route_topk.cuh"
 
 #include <cuda_bf16.h>
 
@@ -46,73 +47,6 @@ constexpr int kMaxE = 1024;          // routed experts
 constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
 constexpr int kPermWarps = 16;       // tokens per permute CTA
 constexpr int kCombineSlots = 10;    // the combine keeps up to this many slots in flight per thread
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Top-k of one token by one warp.  NV = logits held per lane (E <= 32 * NV).
-// Writes ids / weights of token t and returns, in lanes j < k, the j-th
-// selected expert (-1 in the other lanes).
-template <int NV>
-__device__ __forceinline__ int topk_token(const RouteArgs& a, int t, int lane) {
-  const int E = a.E, k = a.k;
-  const float* row = a.logits + static_cast<int64_t>(t) * E;
-  float v[NV];
-  uint32_t taken = 0;  // bit i: value i of this lane is used or absent
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = i * 32 + lane;
-    if (e < E) {
-      v[i] = a.bias ? __fadd_rn(__ldg(row + e), __ldg(a.bias + e)) : __ldg(row + e);
-    } else {
-      v[i] = 0.0f;
-      taken |= 1u << i;
-    }
-  }
-  float sel_v = 0.0f;
-  int sel_e = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      // indices grow with i, so a strict '>' keeps the lower id on ties
-      if (!((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
-        bv = v[i];
-        bi = i * 32 + lane;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const bool better = (oi != 0x7fffffff) && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (better) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) { sel_v = bv; sel_e = bi; }
-  }
-  const float m = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float p = (lane < k) ? expf(sel_v - m) : 0.0f;
-  float denom;
-  if (a.renormalize) {
-    denom = warp_sum(p);
-  } else {
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (i * 32 + lane < E) s += expf(v[i] - m);
-    denom = warp_sum(s);
-  }
-  if (lane < k) {
-    a.ids[static_cast<int64_t>(t) * k + lane] = sel_e;
-    a.weights[static_cast<int64_t>(t) * k + lane] = p / denom;
-  }
-  return sel_e;
-}
 
 template <int NV>
 constexpr int topk_threads() { return NV <= 8 ? 1024 : 512; }
@@ -169,27 +103,6 @@ __global__ void __launch_bounds__(256) route_prefix_kernel(RouteArgs a, int W) {
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) a.counts[e] = carry;
-}
-
-// Exclusive scan over n <= 2048 values held in smem by one warp; returns the total.
-__device__ int warp_exclusive_scan(int* vals, int n, int lane) {
-  const int per = (n + 31) / 32;
-  const int lo = min(n, lane * per), hi = min(n, lo + per);
-  int s = 0;
-  for (int i = lo; i < hi; ++i) s += vals[i];
-  int incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  int run = incl - s;
-  for (int i = lo; i < hi; ++i) {
-    const int c = vals[i];
-    vals[i] = run;
-    run += c;
-  }
-  return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 // Stable position of assignment (t, j) in the expert-sorted order, and the
