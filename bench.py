@@ -210,6 +210,78 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+DENSE_N, DENSE_K = 34816, 5120
+DENSE_M = (1, 16, 64, 256, 1024, 4096)
+
+
+def dense_sweep(args):
+    """The dense NVFP4 W4A4 linear of the pages' second workload: gate_up with
+    N = 34816, K = 5120 for M = 1..4096 tokens.  One call = quantize the BF16
+    activations (TILED_GROUPED, one group) + the grouped GEMM with one group,
+    FP32 out.  The K calls are one CUDA graph; three weight copies (3 x 100 MB,
+    more than L2) rotate so that the weights stream from HBM.  One JSON line
+    per M, with the fraction of the measured HBM copy rate (weights) and of the
+    dense FP4 tensor peak (measured bf16 x 6)."""
+    import nvfp4_moe_grouped_router_gb300 as nvf
+    from nvfp4_moe_grouped_router_gb300 import build as nvf_build
+    torch.cuda.set_device(0)
+    nvf_build.build()
+    nvf.lib()
+    hbm, bf16, src = load_peaks()
+    N, K = DENSE_N, DENSE_K
+    g = torch.Generator(device="cuda").manual_seed(0)
+    copies = []
+    for _ in range(3):
+        w = torch.randn(N, K, generator=g, device="cuda") * 0.02
+        gs_w = torch.tensor([w.abs().max().item() / 2688.0], dtype=torch.float32, device="cuda")
+        B, _ = nvf.quantize(w, gs_w, layout=nvf.LAYOUT_TILED)
+        copies.append((B, gs_w))
+        del w
+    w_bytes = nvf.tiled_bytes(N, 0, K)
+    stream = torch.cuda.Stream()
+    for Mr in DENSE_M:
+        a = torch.randn(Mr, K, generator=g, device="cuda").to(torch.bfloat16)
+        gs_a = torch.tensor([a.float().abs().max().item() / 2688.0], dtype=torch.float32, device="cuda")
+        offs = torch.tensor([0, Mr], dtype=torch.int32, device="cuda")
+        tiles = torch.tensor([0, (Mr + 127) // 128], dtype=torch.int32, device="cuda")
+        A = torch.zeros(nvf.tiled_bytes(Mr, 1, K), dtype=torch.uint8, device="cuda")
+        D = torch.empty(Mr, N, dtype=torch.float32, device="cuda")
+
+        def call(i):
+            B, gs_w = copies[i % 3]
+            nvf.quantize(a, gs_a, layout=nvf.LAYOUT_TILED_GROUPED, offsets=offs, tile_offsets=tiles, codes=A)
+            nvf.grouped_gemm(A, Mr, B, gs_a, gs_w, offs, tiles, N, K, D=D)
+
+        steps = max(3, min(args.steps, 60 if Mr >= 1024 else 300))
+        for i in range(max(3, args.warmup)):
+            call(i)
+        torch.cuda.synchronize()
+        stream.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(steps):
+                call(i)
+        torch.cuda.current_stream().wait_stream(stream)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        code, detail = nvf.device_status()
+        if code != 0:
+            raise RuntimeError(f"device error word {code} at {detail}")
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        tflops = 2.0 * Mr * N * K / (us * 1e-6) / 1e12
+        gbs = (w_bytes + Mr * K * 2 + Mr * N * 4) / (us * 1e-6) / 1e9
+        print(json.dumps({"metric": "dense NVFP4 W4A4 linear (gate_up N=34816 K=5120): us per call", "M": Mr,
+                          "us_per_call": us, "tflops": tflops, "gbs": gbs, "hbm_frac": gbs / hbm,
+                          "tc_frac_fp4": tflops / (6.0 * bf16), "peak_source": src, "steps": steps,
+                          "launches_per_call": 2, "data": "synthetic", "l2": "3 weight copies rotate (300 MB)"}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -220,7 +292,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="plain launches of W + K steps and nothing else (for ncu launch lists / captures)")
+    ap.add_argument("--dense", action="store_true",
+                    help="the dense W4A4 linear sweep (N=34816, K=5120, M=1..4096) instead of the MoE layer")
     args = ap.parse_args()
+    if args.dense:
+        return dense_sweep(args)
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

@@ -160,6 +160,33 @@ def test_dense_linear(nvf, rows):
     assert rel_err(D, ref) <= TOL
 
 
+@pytest.mark.parametrize("rows", [1, 300, 2048])
+def test_dense_linear_pages_shape(nvf, rows):
+    """The dense W4A4 linear at the pages' gate_up shape (N = 34816, K = 5120),
+    through the product path: activations and weights quantized on the GPU, then
+    the grouped GEMM with one group.  The oracle quantizes the same float rows
+    (same global scales, an input here) and computes 256 sampled output columns."""
+    N, K = 34816, 5120
+    g = torch.Generator(device="cuda").manual_seed(4096 + rows)
+    w = torch.randn(N, K, generator=g, device="cuda") * 0.02
+    a = torch.randn(rows, K, generator=g, device="cuda")
+    gs_w = np.float32(F.global_scale(np.float32(w.abs().max().item())))
+    gs_a = np.float32(F.global_scale(np.float32(a.abs().max().item())))
+    dev32 = lambda v: torch.tensor([v], dtype=torch.float32, device="cuda")
+    B, _ = nvf.quantize(w, dev32(gs_w), layout=nvf.LAYOUT_TILED)
+    offs = torch.tensor([0, rows], dtype=torch.int32, device="cuda")
+    tiles = torch.tensor([0, (rows + 127) // 128], dtype=torch.int32, device="cuda")
+    A, _ = nvf.quantize(a, dev32(gs_a), layout=nvf.LAYOUT_TILED_GROUPED, offsets=offs, tile_offsets=tiles)
+    D = nvf.grouped_gemm(A, rows, B, dev32(gs_a), dev32(gs_w), offs, tiles, N, K, torch.float32)
+    code, detail = nvf.device_status()
+    assert code == 0, f"device error word {code} at {detail}"
+    cols = np.sort(np.random.default_rng(rows).choice(N, 256, replace=False))
+    w_c, w_s = F.quantize_rows(w[torch.from_numpy(cols).cuda()].cpu().numpy(), gs_w)
+    a_c, a_s = F.quantize_rows(a.cpu().numpy(), gs_a)
+    ref = M.grouped_gemm(a_c, a_s, np.array([0, rows]), np.array([gs_a]), w_c[None], w_s[None], np.array([gs_w]))
+    assert rel_err(D[:rows].cpu().numpy()[:, cols], ref) <= TOL
+
+
 def test_argument_validation(nvf):
     z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     f = torch.ones(1, dtype=torch.float32, device="cuda")
