@@ -264,29 +264,50 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_small_permute_kernel(Ro
 // once per token, not once per slot).
 enum PermMode : int { PERM_ONLY = 0, PERM_TOKEN = 2 };
 
-__device__ __forceinline__ void load_group64_bf16(const RouteArgs& a, int t, int gg, float (&v)[64]) {
+// 64 BF16 values (K elements 64 gg ..) of row t, kept packed (32 registers).
+__device__ __forceinline__ void load_group64_packed(const RouteArgs& a, int t, int gg, uint4 (&xr)[8]) {
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
                                                     static_cast<int64_t>(t) * a.H + gg * 64);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 u = __ldg(src + i);
-    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+  for (int i = 0; i < 8; ++i) xr[i] = __ldg(src + i);
+}
+
+// Quantize a packed 64-value group one 16-element block at a time (so that only
+// 16 floats are live): 32 code bytes in w, the four scale bytes returned.
+__device__ __forceinline__ uint32_t quant_packed64(const uint4 (&xr)[8], float gs, uint32_t (&w)[8]) {
+  const float six_gs = __fmul_rn(6.0f, gs);
+  uint32_t sf = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[i * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
-      v[i * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+  for (int b = 0; b < 4; ++b) {
+    float v[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = xr[2 * b + h];
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[h * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
+        v[h * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+      }
     }
+    sf |= quant_block16(v, gs, six_gs, w[2 * b], w[2 * b + 1]) << (8 * b);
   }
+  return sf;
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArgs a, int W) {
+__global__ void __launch_bounds__(kPermWarps * 32, 2) route_permute_kernel(RouteArgs a, int W) {
   __shared__ int offs[kMaxE + 2];
   __shared__ int til[kMaxE + 2];
   __shared__ int s_pos[MODE == PERM_TOKEN ? kPermWarps : 1][33];
   __shared__ int s_exp[MODE == PERM_TOKEN ? kPermWarps : 1][33];
   const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kPermWarps + warp;
+  // The token's first 64-value group per lane, fetched before the wait on the
+  // routing kernels (x does not depend on them).
+  uint4 xr[8];
+  if (MODE == PERM_TOKEN && t < T && lane < (a.H >> 6)) load_group64_packed(a, t, lane, xr);
   griddep_wait();
   griddep_launch_dependents();
   // per-expert counts -> expert offsets and tile offsets (every CTA, redundantly)
@@ -314,7 +335,6 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
   }
   __syncthreads();
   if (blockIdx.x == 0 && blockIdx.y == 0) write_offsets(a, offs, til, Et);
-  const int t = blockIdx.x * kPermWarps + warp;
   if (t >= T) return;
   {
     const int slots = k + a.shared;
@@ -334,8 +354,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
       __syncwarp();
       const int gpr = a.H >> 6;
       for (int gg = lane; gg < gpr; gg += 32) {
-        float v[64];
-        load_group64_bf16(a, t, gg, v);
+        if (gg != lane) load_group64_packed(a, t, gg, xr);
         uint32_t w[8];
         uint32_t sf = 0;
         float gs_done = -1.0f;  // global scales are positive
@@ -343,7 +362,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_permute_kernel(RouteArg
           const int ej = s_exp[warp][j], pj = s_pos[warp][j];
           const float gs = __ldg(a.gs_a1 + ej);
           if (gs != gs_done) {
-            sf = quant_group64(v, gs, w);
+            sf = quant_packed64(xr, gs, w);
             gs_done = gs;
           }
           const int local = pj - offs[ej];
