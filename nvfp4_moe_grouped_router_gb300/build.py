@@ -3,8 +3,7 @@
     python -m nvfp4_moe_grouped_router_gb300.build [--force] [-v]
 
 Each translation unit is compiled in parallel; the shared library links the
-CUDA runtime statically and resolves the tensor-map encoder through the
-driver entry-point API, so it needs no libcuda at link time.
+CUDA runtime statically, so it needs no libcuda at link time.
 """
 from __future__ import annotations
 

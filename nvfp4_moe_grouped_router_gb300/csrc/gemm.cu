@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           }
           const uint32_t st = stage_addr(stage);
           const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
-          // scale atoms first: the expanders start on them while the codes arrive
+          // scale atoms first: the scale writers start on them while the codes arrive
           mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
           bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
           for (int h = 0; h < nbt; ++h) {

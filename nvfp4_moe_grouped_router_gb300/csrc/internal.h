@@ -2,7 +2,6 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace nvf {

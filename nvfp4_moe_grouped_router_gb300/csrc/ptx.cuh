@@ -1,10 +1,8 @@
-// Inline-PTX building blocks for sm_103a: mbarriers with bounded waits, TMA
-// (tensor and bulk copies), tcgen05 (TMEM alloc, MMA, copies, loads) and the
-// FP4/FP8 conversion instructions.  Everything here is hand-written PTX; no
-// library headers beyond cuda.h (for CUtensorMap) are used.
+// Inline-PTX building blocks for sm_103a: mbarriers with bounded waits, bulk
+// (TMA engine) copies, tcgen05 (TMEM alloc, MMA, loads) and the FP4/FP8
+// conversion instructions.  Everything here is hand-written PTX.
 #pragma once
 #include <cstdint>
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -98,19 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// ----------------------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
-}
-// 2-D tiled load (x = innermost coordinate in elements, y = row) into shared
-// memory, completing `bar`'s transaction count.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(m), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
+// ----------------------------------------------------------------------------- bulk copies
 // Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -162,16 +148,6 @@ constexpr uint32_t kSwizzleNone = 0, kSwizzle128B = 2;
 __device__ __forceinline__ uint64_t operand_desc_sw128(uint32_t saddr) {
   return smem_desc(saddr, 16, 1024, kSwizzle128B);
 }
-// A 512-byte scale-factor atom (32 rows of 16 bytes, unswizzled).
-__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t saddr) { return smem_desc(saddr, 128, 128, kSwizzleNone); }
-
-// Copy one 32 x 128-bit scale-factor atom into TMEM, replicated to all four
-// 32-lane quarters: lane (i + 32q), column c + j receives bytes [4j, 4j+4) of
-// atom row i.
-__device__ __forceinline__ void tc_copy_sf_atom(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
 // Instruction descriptor of the block-scaled FP4 MMA (kind::mxf4nvf4):
 // A and B E2M1 (format 1) in bits [7,10) and [10,13), both K-major, N >> 3 in
 // [17,23), scale type UE4M3 (bit 23 = 0), M >> 7 in [27,29), scale-factor ids 0.

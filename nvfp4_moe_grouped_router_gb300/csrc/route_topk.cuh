@@ -35,8 +35,7 @@ __device__ __forceinline__ TopkIO topk_io(const RouteArgs& a, bool write) {
   return TopkIO{a.logits, a.bias, a.E, a.k, a.renormalize, write ? a.ids : nullptr, a.weights};
 }
 
-// Top-k of NT tokens by one warp, interleaved so that their latency chains
-// overlap.  Each round takes the warp maximum of the remaining keys with one
+// Top-k of NT tokens by one warp (the routing kernels use NT = 1).  Each round takes the warp maximum of the remaining keys with one
 // redux.sync and the lowest expert id holding it with one ballot per value a
 // lane holds (id = 32 i + lane, so the first i with a hit, then the lowest
 // lane): the largest logit, ties to the lower id.  NV = logits held per lane
