@@ -39,7 +39,7 @@ def row_tiles(rows: int, offsets=None, tile_offsets=None):
     return tile_offsets[g] + local // 128, local % 128
 
 
-def _tiled_index(tile, r, K):
+def tiled_index(tile, r, K):
     """Byte offsets of every code byte [rows, K/2] and scale byte [rows, K/16]."""
     nkt = (K + 255) // 256
     tile = np.asarray(tile, dtype=np.int64)[:, None]
@@ -56,14 +56,14 @@ def _tiled_index(tile, r, K):
 def tiled_unpack(buf, K, tile, r):
     """Tiled operand bytes -> (codes [rows, K/2], scales [rows, K/16]) for rows at (tile, r)."""
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
-    code, sf = _tiled_index(tile, r, K)
+    code, sf = tiled_index(tile, r, K)
     return buf[code], buf[sf]
 
 
 def tiled_pack(codes, scales, K, tile, r, nbytes):
     """Inverse of tiled_unpack; bytes not covered stay 0."""
     out = np.zeros(nbytes, np.uint8)
-    code, sf = _tiled_index(tile, r, K)
+    code, sf = tiled_index(tile, r, K)
     out[code] = codes
     out[sf] = scales
     return out
