@@ -154,6 +154,29 @@ nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t 
                           int32_t G, const float* gscale, uint8_t* codes, uint8_t* scales, int32_t layout,
                           void* stream);
 
+/* Weight preparation (the offline step before the layer runs; not timed).
+ * Turns FP32 or BF16 expert weights into the prepared form nvf_moe_weights
+ * points to, for experts e0 .. e0 + n_experts - 1 (so a caller can stream a
+ * large expert set through a small source buffer):
+ *   w13_src   device [n_experts, 2I, H] of src_dtype: rows [0, I) gate (w1),
+ *             rows [I, 2I) up (w3) of each expert.
+ *   w2_src    device [n_experts, H, I].
+ *   gs_w13, gs_w2  device float[E'] (entries e0 .. e0 + n_experts - 1 written):
+ *             amax(expert) / 2688, or 1 for an all-zero expert.
+ *   w13       device NVF_LAYOUT_TILED buffer of the [E' * 2I, H] stack
+ *             (nvfp4_tiled_bytes(E' * 2I, 0, H) bytes), rows of each expert in
+ *             nvf_w13_row_map order; w2 the NVF_LAYOUT_TILED [E' * H, I] stack.
+ *   H a positive multiple of 128, I of 64; all buffers 16-byte aligned.
+ * Every 16 consecutive input elements of a row become one NVFP4 block as in
+ * nvfp4_quantize.  Source: "FP4 weights with FP8 block scales" per expert
+ * (FlashInfer issue #2723, "Model" table); one FP32 scale per expert that the
+ * grouped GEMM's epilogue folds into a per-expert alpha with beta = 0 (vLLM PR
+ * #29242, review of nvfp4_blockwise_moe_kernel.cu: alpha_ptr_array).
+ * Asynchronous on `stream`; four kernel launches, no allocation. */
+nvf_status nvfp4_prepare_weights(const void* w13_src, const void* w2_src, int32_t src_dtype, int32_t e0,
+                                 int32_t n_experts, int32_t H, int32_t I, uint8_t* w13, float* gs_w13, uint8_t* w2,
+                                 float* gs_w2, void* stream);
+
 /* Top-k routing and permutation (steps 1-2).
  *   logits       device float[T, E]; bias device float[E] or NULL, added in FP32.
  *   T >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32); renormalize: softmax over
@@ -172,7 +195,8 @@ nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, 
                              int32_t* src_to_perm, int32_t* perm_token, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_route_permute for callers that cannot allocate device memory.  (The
- * source pages have no counterpart: this is a library convenience.)
+ * source pages have no counterpart to this entry point: it is a library
+ * convenience, not a step of the method.)
  * Some callers have no way to hand this library scratch memory: code that runs
  * inside a framework whose caching allocator owns every device allocation,
  * plug-ins that are given only their input and output buffers, or
@@ -181,10 +205,13 @@ nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, 
  * same inputs and outputs as moe_route_permute but no workspace: its scratch
  * is a fixed 2 MiB array in device memory that the library reserves on every
  * GPU that loads it, for the life of the process.
- *   - Sizes: the scratch needed (moe_route_permute_workspace_size(T, E)) must
- *     not exceed NVF_ROUTE_STATIC_SCRATCH_BYTES; larger calls return
- *     NVF_ERR_WORKSPACE before any launch (about T*E <= 2^24, e.g. 65536 tokens
- *     with 256 experts).
+ *   - Sizes: the scratch a call needs, moe_route_permute_workspace_size(T, E)
+ *     = (2 * ceil(T / 32) * E + E) * 4 bytes rounded up to a multiple of 256,
+ *     must not exceed NVF_ROUTE_STATIC_SCRATCH_BYTES (2 MiB); larger calls
+ *     return NVF_ERR_WORKSPACE before any launch.  That allows T <= 65504
+ *     tokens with 128 experts, T <= 32736 with 256, T <= 8160 with 1024.
+ *     Device and argument checks come first and return what moe_route_permute
+ *     returns (NVF_ERR_UNSUPPORTED_DEVICE, NVF_ERR_INVALID_ARG).
  *   - Allocation: none.  No cudaMalloc/cudaFree or allocating library call is
  *     made.  The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
@@ -232,7 +259,8 @@ typedef struct nvf_moe_ws_layout {
   size_t tile_group;        /* int32[R/128 + E' + 1]: expert of each 128-row tile of A1 / A2 */
   size_t a1;                /* NVF_LAYOUT_TILED_GROUPED, K = H */
   size_t a2;                /* NVF_LAYOUT_TILED_GROUPED, K = I */
-  size_t y;                 /* float[R, H], row = permuted slot */
+  size_t y;                 /* [R, H], row = permuted slot: float when the forward's out is NVF_F32, bf16
+                               when it is NVF_BF16 (the region is sized for float) */
   size_t total;
   int64_t R;                /* rows after permutation */
 } nvf_moe_ws_layout;
@@ -240,7 +268,10 @@ typedef struct nvf_moe_ws_layout {
 nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I, int32_t k, int32_t shared,
                                       nvf_moe_ws_layout* layout);
 
-/* The whole layer (steps 1-7) on one stream.
+/* The whole layer (steps 1-7) on one stream.  The down GEMM's output y (one row per
+ * permuted slot) is kept in the output's precision: FP32 with an NVF_F32 out (the
+ * parity setting), BF16 with an NVF_BF16 out (half the bytes of the y round trip);
+ * the combine sums the k slots in slot order in FP32 either way and rounds once.
  *   x        device bf16[T, H]; logits device float[T, E]; bias NULL or float[E].
  *   gs_a1, gs_a2 device float[E']: static activation global scales.
  *   out      device [T, H] of out_dtype (NVF_F32 | NVF_BF16).

@@ -34,6 +34,7 @@ SIGNATURES = {
     "nvfp4_tiled_bytes": (_SZ, [_I64, _I32, _I32]),
     "nvfp4_global_scale": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I32, _I64, _I32, _I64, _P, _P, _P, _I32, _P, _P, _P, _I32, _P]),
+    "nvfp4_prepare_weights": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "moe_route_permute_workspace_size": (ctypes.c_int, [_I32, _I32, ctypes.POINTER(_SZ)]),
     "moe_route_permute": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                          _SZ, _P]),
@@ -221,30 +222,30 @@ class MoEWeights:
                            self.w2.data_ptr(), self.gs_w2.data_ptr())
 
 
-def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="cuda") -> MoEWeights:
-    """Quantize FP32 expert weights on the device into the layer's layout.
+def prepare_weights(E: int, H: int, I: int, shared: bool, expert_fp32, device="cuda", chunk: int = 16) -> MoEWeights:
+    """Prepare expert weights on the device with nvfp4_prepare_weights.
 
-    expert_fp32(e) -> (w13 [2I, H], w2 [H, I]) float32 tensors on `device` (gate rows
-    first, then up rows).  Per expert: gs = amax / 2688, NVFP4 rows along the
-    input dimension, w13 rows reordered by w13_row_map, TILED layout.
+    expert_fp32(e) -> (w13 [2I, H], w2 [H, I]) float32 tensors (gate rows first,
+    then up rows).  Experts are staged `chunk` at a time into one FP32 buffer
+    and handed to the library, which computes the per-expert global scales, the
+    NVFP4 rows, the w13 row order and the TILED layout.
     """
     Et = E + int(shared)
-    n13, n2 = tiled_bytes(2 * I, 0, H), tiled_bytes(H, 0, I)     # one expert's chunks
-    w13 = torch.zeros(Et * n13, dtype=torch.uint8, device=device)
-    w2 = torch.zeros(Et * n2, dtype=torch.uint8, device=device)
+    w13 = torch.zeros(tiled_bytes(Et * 2 * I, 0, H), dtype=torch.uint8, device=device)
+    w2 = torch.zeros(tiled_bytes(Et * H, 0, I), dtype=torch.uint8, device=device)
     gs13 = torch.empty(Et, dtype=torch.float32, device=device)
     gs2 = torch.empty(Et, dtype=torch.float32, device=device)
-    rmap = torch.tensor(w13_row_map(I), dtype=torch.int32, device=device)
-    for e in range(Et):
-        a, b = expert_fp32(e)
-        a = a.to(device=device, dtype=torch.float32).contiguous()
-        b = b.to(device=device, dtype=torch.float32).contiguous()
-        g13 = global_scale(a)
-        g2 = global_scale(b)
-        gs13[e:e + 1].copy_(g13)
-        gs2[e:e + 1].copy_(g2)
-        quantize(a, g13, LAYOUT_TILED, gather=rmap, codes=w13[e * n13:(e + 1) * n13])
-        quantize(b, g2, LAYOUT_TILED, codes=w2[e * n2:(e + 1) * n2])
+    n = max(1, min(chunk, Et))
+    s13 = torch.empty(n, 2 * I, H, dtype=torch.float32, device=device)
+    s2 = torch.empty(n, H, I, dtype=torch.float32, device=device)
+    for e0 in range(0, Et, n):
+        m = min(n, Et - e0)
+        for i in range(m):
+            a, b = expert_fp32(e0 + i)
+            s13[i].copy_(a)
+            s2[i].copy_(b)
+        _check(lib().nvfp4_prepare_weights(_ptr(s13), _ptr(s2), NVF_F32, e0, m, H, I, _ptr(w13), _ptr(gs13),
+                                           _ptr(w2), _ptr(gs2), _stream()))
     return MoEWeights(E, H, I, shared, w13, gs13, w2, gs2)
 
 

@@ -189,6 +189,27 @@ __global__ void selftest_wait_kernel(int* err, uint64_t limit_ns) {
 }
 }  // namespace nvf
 
+static nvf_status validate_route(int32_t T, int32_t E, int32_t k, int32_t shared) {
+  NVF_REQUIRE(T >= 0 && T <= (1 << 24), "T=%d must be in [0, 2^24]", T);
+  NVF_REQUIRE(E >= 1 && E <= 1024, "E=%d must be in [1, 1024]", E);
+  NVF_REQUIRE(k >= 1 && k <= E && k <= 32, "k=%d must be in [1, min(E=%d, 32)]", k, E);
+  NVF_REQUIRE(shared == 0 || shared == 1, "shared_expert=%d must be 0 or 1", shared);
+  NVF_REQUIRE(static_cast<int64_t>(T) * (k + shared) < (int64_t(1) << 31), "T*(k+shared) overflows int32");
+  return NVF_OK;
+}
+
+namespace nvf {
+// The checks moe_route_permute_noalloc makes before it touches its fixed
+// scratch: the same device check and argument checks as moe_route_permute, in
+// the same order, so that both entry points return the same status for the
+// same fault.
+nvf_status route_precheck(int32_t T, int32_t E, int32_t k, int32_t shared) {
+  NVF_BEGIN();
+  (void)dev_;
+  return validate_route(T, E, k, shared);
+}
+}  // namespace nvf
+
 extern "C" {
 
 nvf_status nvf_selftest_bounded_wait(uint64_t limit_ns, void* stream) {
@@ -204,10 +225,7 @@ nvf_status nvf_w13_row_map(int32_t I, int32_t* map) {
   g_msg[0] = 0;
   NVF_REQUIRE(I > 0 && I % 64 == 0, "I=%d must be a positive multiple of 64", I);
   NVF_REQUIRE(map != nullptr, "map must not be NULL");
-  for (int32_t r = 0; r < 2 * I; ++r) {
-    const int32_t c = r / 32, within = r % 32;
-    map[r] = within < 16 ? 16 * c + within : I + 16 * c + (within - 16);
-  }
+  for (int32_t r = 0; r < 2 * I; ++r) map[r] = static_cast<int32_t>(w13_source_row(r, I));
   return NVF_OK;
 }
 
@@ -252,6 +270,40 @@ nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t 
   return NVF_OK;
 }
 
+nvf_status nvfp4_prepare_weights(const void* w13_src, const void* w2_src, int32_t src_dtype, int32_t e0,
+                                 int32_t n_experts, int32_t H, int32_t I, uint8_t* w13, float* gs_w13, uint8_t* w2,
+                                 float* gs_w2, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(w13_src && w2_src && w13 && gs_w13 && w2 && gs_w2, "weight pointers must not be NULL");
+  NVF_REQUIRE(src_dtype == NVF_F32 || src_dtype == NVF_BF16, "src_dtype=%d must be NVF_F32 or NVF_BF16", src_dtype);
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(I > 0 && I % 64 == 0, "I=%d must be a positive multiple of 64", I);
+  NVF_REQUIRE(e0 >= 0 && n_experts >= 1 && n_experts <= 65535, "e0=%d must be >= 0 and n_experts=%d in [1, 65535]",
+              e0, n_experts);
+  NVF_REQUIRE(static_cast<int64_t>(e0 + n_experts) * 2 * I * H < (int64_t(1) << 40), "weight stack too large");
+  NVF_REQUIRE(aligned16(w13_src) && aligned16(w2_src) && aligned16(w13) && aligned16(w2),
+              "w13_src, w2_src, w13 and w2 must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t rows13 = static_cast<int64_t>(n_experts) * 2 * I, rows2 = static_cast<int64_t>(n_experts) * H;
+  // per-expert global scales gs = amax / 2688 (1 for an all-zero expert)
+  NVF_CUDA(launch_global_scale(w13_src, src_dtype, n_experts, int64_t(2) * I * H, gs_w13 + e0, s), "w13 global scales");
+  NVF_CUDA(launch_global_scale(w2_src, src_dtype, n_experts, int64_t(H) * I, gs_w2 + e0, s), "w2 global scales");
+  // NVFP4 rows along the input dimension into the TILED layout; w13 rows in the
+  // order the fused SiLU-and-mul epilogue reads them.  Expert boundaries fall on
+  // 128-row tiles (2I and H are multiples of 128), so expert e starts at chunk
+  // e * rows / 128 * nkt of each buffer.
+  QuantArgs a13{w13_src, src_dtype, rows13, H, H, nullptr, nullptr, nullptr, 1, gs_w13 + e0,
+                w13 + nvfp4_tiled_bytes(static_cast<int64_t>(e0) * 2 * I, 0, H), nullptr, LAYOUT_TILED};
+  a13.rows_per_group = 2 * I;
+  a13.w13_I = I;
+  NVF_CUDA(launch_quantize(a13, s), "w13 quantize");
+  QuantArgs a2{w2_src, src_dtype, rows2, I, I, nullptr, nullptr, nullptr, 1, gs_w2 + e0,
+               w2 + nvfp4_tiled_bytes(static_cast<int64_t>(e0) * H, 0, I), nullptr, LAYOUT_TILED};
+  a2.rows_per_group = H;
+  NVF_CUDA(launch_quantize(a2, s), "w2 quantize");
+  return NVF_OK;
+}
+
 nvf_status moe_route_permute_workspace_size(int32_t T, int32_t E, size_t* bytes) {
   g_msg[0] = 0;
   NVF_REQUIRE(bytes != nullptr && T >= 0 && E >= 1, "bad arguments");
@@ -260,14 +312,6 @@ nvf_status moe_route_permute_workspace_size(int32_t T, int32_t E, size_t* bytes)
   return NVF_OK;
 }
 
-static nvf_status validate_route(int32_t T, int32_t E, int32_t k, int32_t shared) {
-  NVF_REQUIRE(T >= 0 && T <= (1 << 24), "T=%d must be in [0, 2^24]", T);
-  NVF_REQUIRE(E >= 1 && E <= 1024, "E=%d must be in [1, 1024]", E);
-  NVF_REQUIRE(k >= 1 && k <= E && k <= 32, "k=%d must be in [1, min(E=%d, 32)]", k, E);
-  NVF_REQUIRE(shared == 0 || shared == 1, "shared_expert=%d must be 0 or 1", shared);
-  NVF_REQUIRE(static_cast<int64_t>(T) * (k + shared) < (int64_t(1) << 31), "T*(k+shared) overflows int32");
-  return NVF_OK;
-}
 
 nvf_status moe_route_permute(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k,
                              int32_t renormalize, int32_t shared_expert, int32_t* topk_ids, float* topk_w,
@@ -396,9 +440,17 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = static_cast<uint8_t*>(ws);
   auto i32 = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
+  // Stage events: while the stream is being captured into a graph they are
+  // recorded as external event nodes (so that the graph records them at replay);
+  // otherwise they are plain records.
+  unsigned int ev_flags = cudaEventRecordDefault;
+  if (stage_events) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    NVF_CUDA(cudaStreamIsCapturing(s, &cs), "cudaStreamIsCapturing");
+    if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) -> cudaError_t {
-    // External records become event nodes when the stream is being captured into a graph.
-    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, cudaEventRecordExternal)
+    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, ev_flags)
                         : cudaSuccess;
   };
   NVF_CUDA(mark(0), "cudaEventRecord");
@@ -443,16 +495,24 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   g2.offsets = i32(L.expert_offsets); g2.tile_offs = i32(L.tile_offsets); g2.G = Et; g2.N = H; g2.K = I;
   g2.tile_group = i32(L.tile_group);
   g2.small_a = T <= 32;
-  g2.epilogue = EPI_STORE_F32; g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
+  // y has the output's type: FP32 for parity runs, BF16 for production (half the
+  // bytes of the y round trip through HBM; the combine still sums in FP32)
+  g2.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
+  g2.d = base + L.y; g2.ldd = H; g2.err = dev_->err;
   g2.d_align32 = true;  // 256-byte aligned workspace, H a multiple of 128
-  g2.pdl = pdl; g2.early_weights = pdl;  // expert offsets come from the route, two kernels back
+  // With programmatic dependent launch the down GEMM may begin before the gate_up
+  // GEMM ends and prefetch its first weight tile before its own dependency wait.
+  // The group tables it reads for that come from the routing kernel, two launches
+  // back; they are already complete: the gate_up GEMM executes its dependency
+  // wait on the routing kernel before it allows this launch to begin.
+  g2.pdl = pdl; g2.early_weights = pdl;
   e = launch_grouped_gemm(g2, s, &why);
   if (e != cudaSuccess)
     return fail(NVF_ERR_CUDA, "down GEMM (E'=%d R=%lld N=%d K=%d): %s", Et, (long long)L.R, H, I,
                 why ? why : cudaGetErrorString(e));
   NVF_CUDA(mark(4), "cudaEventRecord");
 
-  NVF_CUDA(launch_combine(reinterpret_cast<const float*>(base + L.y), H, reinterpret_cast<const float*>(base + L.topk_w),
+  NVF_CUDA(launch_combine(base + L.y, H, reinterpret_cast<const float*>(base + L.topk_w),
                           i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s, pdl),
            "combine launch");
   NVF_CUDA(mark(5), "cudaEventRecord");

@@ -18,17 +18,18 @@
 // them with tcgen05.st in the layout the MMA reads (each quarter holds its own
 // copy of B's scales; A row r's scales sit in lane r).
 //
-// Roles (one CTA per SM, persistent, 448 threads):
+// Roles (one CTA per SM, persistent, 512 threads = four warpgroups; setmaxnreg
+// gives the epilogue warpgroups 192 registers a thread, the others 64 and 56):
 //   warps 0-3   scale writers: as soon as a stage's scale atoms have landed
 //               (while its codes are still arriving), load them from shared
 //               memory and store them into the stage's TMEM scale slot (warp q
 //               writes lanes 32q..32q+31), then signal sf_ready.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, 128 columns
-//               each.  They move the accumulator to registers and release it
-//               at once (the next tile's MMAs start), then apply
-//               alpha and store FP32/BF16 rows, or h = silu(gate) * up
-//               requantized to NVFP4 straight into the next GEMM's tiled
-//               operand.
+//               each.  They move their whole slice of the accumulator to
+//               registers and release it before any arithmetic, so the next
+//               tile's MMAs run while this tile is finished: alpha and
+//               FP32/BF16 rows, or h = silu(gate) * up requantized to NVFP4
+//               straight into the next GEMM's tiled operand.
 //   warp 12     producer: per K tile the scale atoms of the A chunk and of the
 //               two B chunks of the tile's 256 weight rows (first, on their own
 //               barrier), then the A codes (valid-row prefix) and the B codes,
@@ -39,6 +40,7 @@
 //   warp 13     MMA issuer: per K tile, once the codes have landed and the
 //               scales are in TMEM, four 128x256x64 MMAs into the single
 //               256-column TMEM accumulator.
+//   warps 14-15 idle (they complete warpgroup 3).
 // Every mbarrier wait is bounded; on timeout the kernel records an error word,
 // drains what it issued, frees TMEM and returns.
 #include "internal.h"
@@ -53,12 +55,22 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int SF_WARPS = 4;               // warps 0-3: scale writers, one per TMEM lane quarter
-constexpr int EPI_WARP0 = SF_WARPS;        // warps 4-11: epilogue
+constexpr int SF_WARPS = 4;               // warps 0-3 (warpgroup 0): scale writers, one per TMEM lane quarter
+constexpr int EPI_WARP0 = SF_WARPS;        // warps 4-11 (warpgroups 1-2): epilogue
 constexpr int EPI_WARPS = 8;
-constexpr int PRODUCER_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int PRODUCER_WARP = EPI_WARP0 + EPI_WARPS;  // warpgroup 3: producer, MMA issuer and two idle warps
 constexpr int MMA_WARP = PRODUCER_WARP + 1;
-constexpr int THREADS = 32 * (MMA_WARP + 1);
+constexpr int THREADS = 512;
+// Registers per thread.  The block is launched with 65536 / 512 = 128 a thread;
+// setmaxnreg then moves registers from the scale writers and the control
+// warpgroup to the two epilogue warpgroups, whose threads hold a whole
+// 128-column slice of the accumulator.  The shares must add up to at most the
+// launch's total (a larger request would wait forever), which the host checks
+// against the compiled register count before every launch.
+constexpr int REG_LAUNCH = 128;
+constexpr int REG_SF = 64, REG_CTRL = 56, REG_EPI = 192;
+static_assert(REG_SF + REG_CTRL + 2 * REG_EPI <= 4 * REG_LAUNCH, "register split exceeds the launch's registers");
+static_assert(THREADS * REG_LAUNCH <= 65536, "launch register budget");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = BN;          // scale slots after the accumulator
 constexpr uint32_t SF_SLOT_COLS = 48;     // A: 16 columns, B: 32 columns
@@ -74,9 +86,13 @@ constexpr int SMEM_GROUPS = 1025;
 // faster (its pace is the ring's round-trip time, not the bytes per stage).
 // The MMA still reads 128 A rows; in the small layout rows 32..127 fall on the
 // stage's other bytes and give accumulator rows that are never stored.
-template <bool SMALL_A>
+// STAGING: the store epilogue of large groups stages each warp's output through
+// shared memory (4 KB a warp) so that global stores cover whole 128-byte lines;
+// the space comes from a fourth ring stage (a store GEMM's K is short: the down
+// GEMM has 3 K tiles a tile).
+template <bool SMALL_A, bool STAGING = false>
 struct Smem {
-  static constexpr int STAGES = SMALL_A ? 5 : 4;
+  static constexpr int STAGES = SMALL_A ? 5 : (STAGING ? 3 : 4);
   static constexpr int A_ROWS = SMALL_A ? 32 : BM;
   static constexpr int ST_A = 0;
   static constexpr int ST_ASF = A_ROWS * 128;
@@ -87,7 +103,9 @@ struct Smem {
   static constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
   static constexpr int NUM_BARS = 4 * STAGES + 3;  // full, empty, sf_full, sf_ready per stage; acc_full/empty, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr int STG_WARP_BYTES = 4096;        // 32 rows x 128 bytes
+  static constexpr int OFF_STG = (OFF_MISC + 16 + 127) & ~127;
+  static constexpr int BYTES = (STAGING ? OFF_STG + EPI_WARPS * STG_WARP_BYTES : OFF_MISC + 16) + 1024;  // + alignment slack
   static_assert(SF_COL0 + STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(BYTES <= 227 * 1024, "shared memory budget");
   static_assert(STAGE_BYTES % 1024 == 0 && ST_B % 1024 == 0, "1024-byte alignment");
@@ -200,9 +218,27 @@ __device__ __forceinline__ void load_atom_rows(uint32_t (&v)[16], const uint8_t*
   }
 }
 
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory"); }
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory"); }
+
+template <int EPI, bool SMALL_A>
+constexpr bool staged_store() { return EPI != EPI_SWIGLU_QUANT && !SMALL_A; }
+
+// 16 bytes to / from shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 template <int EPI, bool SMALL_A>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs p) {
-  using SM = Smem<SMALL_A>;
+  using SM = Smem<SMALL_A, staged_store<EPI, SMALL_A>()>;
   constexpr int STAGES = SM::STAGES;
   constexpr int ST_A = SM::ST_A, ST_ASF = SM::ST_ASF, ST_B = SM::ST_B, ST_BSF = SM::ST_BSF;
   constexpr int STAGE_BYTES = SM::STAGE_BYTES, OFF_GRP = SM::OFF_GRP;
@@ -247,11 +283,18 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const int nkt = (k64 + 3) >> 2;
   if (p.early_weights && threadIdx.x == 0) {
     // The previous kernel (which produces A) may still be running: start pulling
-    // this CTA's first weight tile into L2 meanwhile.
+    // this CTA's first weight tile into L2 meanwhile.  The group tables read here
+    // come from the routing kernel two launches back, not from the kernel this
+    // one depends on: they are complete because that kernel (the gate_up GEMM)
+    // executed its own dependency wait on the routing kernel before it allowed
+    // this launch to begin.  The expert and weight tile are clamped to the
+    // weight buffer all the same, so a prefetch can never leave it.
     const Sched sc0 = make_sched(p);
     if (static_cast<int>(blockIdx.x) < sc0.total) {
       const Tile x = decode_tile(blockIdx.x, p, sc0);
-      const uint8_t* bc = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
+      const int g = min(max(x.g, 0), p.G - 1);
+      const int nt0 = min(max(x.nt0, 0), ntiles - (x.wide ? 2 : 1));
+      const uint8_t* bc = p.b + (static_cast<size_t>(g) * ntiles + nt0) * nkt * TILE_BYTES;
       bulk_prefetch_l2(bc, static_cast<uint32_t>(nkt) * TILE_BYTES);
       if (x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, static_cast<uint32_t>(nkt) * TILE_BYTES);
     }
@@ -272,106 +315,113 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const Sched sc = make_sched(p);
   const int total = sc.total;
 
-  if (warp == PRODUCER_WARP) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      int stage = 0;
-      uint32_t ph = 0;
-      uint32_t pending = 0, pend_par = 0;  // per stage: load issued, parity of that phase
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile x = decode_tile(t, p, sc, gr);
-        const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
-        const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
-        const int nbt = x.wide ? 2 : 1;
-        // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
-        int a_rows = x.rows;
-        if (a_rows > SM::A_ROWS) {  // the caller promised at most 32 rows per group
-          report_error(p.err, DEV_BAD_OFFSETS, t);
-          a_rows = SM::A_ROWS;
-        }
-        const uint32_t a_code_bytes = static_cast<uint32_t>((a_rows + 7) & ~7) * 128u;
-        for (int kt = 0; kt < nkt; ++kt) {
-          if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
-            ok = false;
-            break;
+  // Roles by warpgroup; each warpgroup first takes its share of the register
+  // file (every thread of the warpgroup executes the same setmaxnreg).
+  const int wg = warp >> 2;
+  if (wg == 3) {
+    regs_dec<REG_CTRL>();
+    if (warp == PRODUCER_WARP) {
+      if (lane == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t pending = 0, pend_par = 0;  // per stage: load issued, parity of that phase
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          const Tile x = decode_tile(t, p, sc, gr);
+          const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
+          const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
+          const int nbt = x.wide ? 2 : 1;
+          // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
+          int a_rows = x.rows;
+          if (a_rows > SM::A_ROWS) {  // the caller promised at most 32 rows per group
+            report_error(p.err, DEV_BAD_OFFSETS, t);
+            a_rows = SM::A_ROWS;
           }
-          const uint32_t st = stage_addr(stage);
-          const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
-          // scale atoms first: the scale writers start on them while the codes arrive
-          mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
-          bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
-          for (int h = 0; h < nbt; ++h) {
-            const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
-            bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
-          }
-          mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + nbt * TILE_CODE_BYTES);
-          bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
-          for (int h = 0; h < nbt; ++h) {
-            const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
-            bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
-          }
-          pending |= 1u << stage;
-          pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (!ok || *abort_flag) {
-        // Let every copy this thread issued land before the CTA goes away.
-        for (int s = 0; s < STAGES; ++s)
-          if ((pending >> s) & 1u) {
-            mbar_wait_drain(sffull_bar(s), (pend_par >> s) & 1u, p.err, s);
-            mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
-          }
-      }
-    }
-  } else if (warp == MMA_WARP) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      int i = 0;  // K tiles consumed so far (ring position)
-      int tile_i = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
-        const Tile x = decode_tile(t, p, sc, gr);
-        const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
-        for (int kt = 0; kt < nkt; ++kt, ++i) {
-          const int s = i % STAGES;
-          // Stage landed and its scales are in TMEM slot s (written after the
-          // MMAs of K tile i - STAGES, which last read the slot, completed).
-          if (!mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t) ||
-              !mbar_wait(sfready_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
-            ok = false;
-            break;
-          }
-          if (kt == 0) {
-            // the epilogue has moved the previous tile out of TMEM
-            if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+          const uint32_t a_code_bytes = static_cast<uint32_t>((a_rows + 7) & ~7) * 128u;
+          for (int kt = 0; kt < nkt; ++kt) {
+            if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
               ok = false;
               break;
             }
+            const uint32_t st = stage_addr(stage);
+            const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
+            // scale atoms first: the scale writers start on them while the codes arrive
+            mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
+            bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
+            for (int h = 0; h < nbt; ++h) {
+              const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
+              bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
+            }
+            mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + nbt * TILE_CODE_BYTES);
+            bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
+            for (int h = 0; h < nbt; ++h) {
+              const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
+              bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
+            }
+            pending |= 1u << stage;
+            pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              ph ^= 1u;
+            }
           }
-          tc_fence_after();
-          const int na = min(4, k64 - kt * 4);
-          const uint32_t st = stage_addr(s);
-          const uint32_t sf = tmem + SF_COL0 + s * SF_SLOT_COLS;
-          for (int kk = 0; kk < na; ++kk) {
-            const uint32_t sfa = sf + kk * 4;
-            const uint32_t sfb = sf + 16 + (x.wide ? kk * 8 : kk * 4);
-            tc_mma_nvfp4(tmem, operand_desc_sw128(st + ST_A + kk * 32), operand_desc_sw128(st + ST_B + kk * 32),
-                         idesc, sfa, sfb, (kt | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty_bar(s));
         }
-        if (ok) tc_commit(accf_bar);
+        if (!ok || *abort_flag) {
+          // Let every copy this thread issued land before the CTA goes away.
+          for (int s = 0; s < STAGES; ++s)
+            if ((pending >> s) & 1u) {
+              mbar_wait_drain(sffull_bar(s), (pend_par >> s) & 1u, p.err, s);
+              mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
+            }
+        }
       }
-      // Every MMA this thread issued must finish before TMEM is freed.
-      tc_commit(drain_mma_bar);
-      mbar_wait_drain(drain_mma_bar, 0, p.err, -1);
-    }
-  } else if (warp < SF_WARPS) {
+    } else if (warp == MMA_WARP) {
+      if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        int i = 0;  // K tiles consumed so far (ring position)
+        int tile_i = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i) {
+          const Tile x = decode_tile(t, p, sc, gr);
+          const uint32_t idesc = mxf4nvf4_idesc(BM, x.wide ? 256 : 128);
+          for (int kt = 0; kt < nkt; ++kt, ++i) {
+            const int s = i % STAGES;
+            // Stage landed and its scales are in TMEM slot s (written after the
+            // MMAs of K tile i - STAGES, which last read the slot, completed).
+            if (!mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t) ||
+                !mbar_wait(sfready_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+              ok = false;
+              break;
+            }
+            if (kt == 0) {
+              // the epilogue has moved the previous tile out of TMEM
+              if (!mbar_wait(acce_bar, (tile_i & 1) ^ 1u, abort_flag, p.err, DEV_TIMEOUT_MMA, t)) {
+                ok = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const int na = min(4, k64 - kt * 4);
+            const uint32_t st = stage_addr(s);
+            const uint32_t sf = tmem + SF_COL0 + s * SF_SLOT_COLS;
+            for (int kk = 0; kk < na; ++kk) {
+              const uint32_t sfa = sf + kk * 4;
+              const uint32_t sfb = sf + 16 + (x.wide ? kk * 8 : kk * 4);
+              tc_mma_nvfp4(tmem, operand_desc_sw128(st + ST_A + kk * 32), operand_desc_sw128(st + ST_B + kk * 32),
+                           idesc, sfa, sfb, (kt | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(empty_bar(s));
+          }
+          if (ok) tc_commit(accf_bar);
+        }
+        // Every MMA this thread issued must finish before TMEM is freed.
+        tc_commit(drain_mma_bar);
+        mbar_wait_drain(drain_mma_bar, 0, p.err, -1);
+      }
+    }  // warps 14-15 have no role
+  } else if (wg == 0) {
+    regs_dec<REG_SF>();
     // -------------------------------------------------------------- scale writers
     const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lane quarter
     int i = 0;
@@ -422,6 +472,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       }
     }
   } else {
+    regs_inc<REG_EPI>();
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int half = (warp - EPI_WARP0) >> 2;  // which 128 of the tile's 256 columns
@@ -445,25 +496,34 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar);  // accumulator is in registers: release it
       };
+      // The whole 128-column slice of the accumulator moves to registers (128
+      // values a thread: the epilogue warpgroups run with REG_EPI registers) and
+      // the accumulator is released before any arithmetic, so the next tile's
+      // MMAs run while this tile is scaled, quantized and stored.
+      uint32_t v[4][32];
+      if (active) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tb + c * 32, v[c]);
+        tmem_ld_wait();
+      }
+      release();
+      if (!active) continue;
       if constexpr (EPI == EPI_SWIGLU_QUANT) {
         // Prepared w13 rows: in every 32-column chunk c of weight tile nt, the
         // first 16 columns are gate rows and the last 16 the matching up rows
-        // of intermediate indices nt * 64 + 16 c .. + 15.  Chunks 0-1 are
-        // loaded; each quantized chunk's registers take the next chunk, and the
-        // accumulator is released once chunk 3 is in: at most 64 accumulator
-        // values are live, so nothing spills to (L2-backed) local memory.
+        // of intermediate indices nt * 64 + 16 c .. + 15.
         const int I = p.N >> 1;
         const float six_gsq = __fmul_rn(6.0f, gsq);
-        uint32_t v[2][32];
         uint32_t cw[8];
         uint32_t sfw = 0;
-        auto block = [&](const uint32_t (&a)[32], int c) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           float h[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             // rows past the group's end carry whatever their scale bytes held: use zeros
-            const float g = valid ? __fmul_rn(__uint_as_float(a[j]), alpha) : 0.0f;
-            const float u = valid ? __fmul_rn(__uint_as_float(a[16 + j]), alpha) : 0.0f;
+            const float g = valid ? __fmul_rn(__uint_as_float(v[c][j]), alpha) : 0.0f;
+            const float u = valid ? __fmul_rn(__uint_as_float(v[c][16 + j]), alpha) : 0.0f;
             h[j] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
           }
           if (p.h_dump != nullptr && valid) {
@@ -472,22 +532,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             for (int j = 0; j < 4; ++j) hd[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
           }
           sfw |= quant_block16(h, gsq, six_gsq, cw[2 * c], cw[2 * c + 1]) << (8 * c);
-        };
-        if (active) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) tmem_ld32(tb + c * 32, v[c]);
-          tmem_ld_wait();
-          block(v[0], 0);
-          tmem_ld32(tb + 64, v[0]);
-          tmem_ld_wait();
-          block(v[1], 1);
-          tmem_ld32(tb + 96, v[1]);
-          tmem_ld_wait();
         }
-        release();
-        if (!active) continue;
-        block(v[0], 2);
-        block(v[1], 3);
         // A2 is the down GEMM's A operand (TILED_GROUPED, K = I): weight tile
         // nt's 64 h values are MMA step nt % 4 of K tile nt / 4: 32 code bytes
         // and 4 scale bytes of row r.
@@ -499,55 +544,89 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
               make_uint4(cw[4], cw[5], cw[6], cw[7]);
         }
         *reinterpret_cast<uint32_t*>(chunk + TILE_CODE_BYTES + (nt & 3) * 512 + sf_atom_offset(r, 0)) = sfw;
-      } else {
-        // Two passes of 64 columns: the first pass's stores go out before the
-        // second pass's loads, so only 64 accumulator values are ever live.
+      } else if constexpr (staged_store<EPI, SMALL_A>()) {
+        // Each 128-byte column chunk of the warp's 32 rows goes through its 4 KB
+        // of shared memory: lane l writes its row's eight 16-byte pieces (piece j
+        // at l * 128 + ((j ^ (l % 8)) * 16), so that the writes and the reads
+        // below hit distinct banks), then each store instruction writes four
+        // whole rows' 128 bytes: lane l takes piece l % 8 of row 4 i + l / 8.
+        constexpr bool F32 = EPI == EPI_STORE_F32;
+        constexpr int CHUNK_COLS = F32 ? 32 : 64;             // 128 bytes of a row
+        const uint32_t stg = s_base + SM::OFF_STG + static_cast<uint32_t>((warp - EPI_WARP0) * SM::STG_WARP_BYTES);
+        const int rows_here = min(32, x.rows - q * 32);       // valid rows of this warp's quarter
 #pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          uint32_t v[2][32];
-          if (active) {
+        for (int ch = 0; ch < 128 / CHUNK_COLS; ++ch) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tmem_ld32(tb + pass * 64 + c * 32, v[c]);
-            tmem_ld_wait();
-          }
-          if (pass == 1) release();
-          if (!active || !valid) continue;
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
+            if constexpr (F32) {
+              const int c = ch, e0 = 4 * j;                     // columns 32 ch + 4 j .. + 3
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int64_t col = static_cast<int64_t>(nt) * 128 + pass * 64 + c * 32;
-            if constexpr (EPI == EPI_STORE_F32) {
-              float* drow = static_cast<float*>(p.d) + row * p.ldd + col;
-              if (p.d_align32) {
-                // whole 32-byte sectors per instruction
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint32_t o[8];
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][8 * j + e]), alpha));
-                  st_global_v8(drow + 8 * j, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
-                }
-              } else {
-                float4* dst = reinterpret_cast<float4*>(drow);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  dst[j] = make_float4(__fmul_rn(__uint_as_float(v[c][4 * j]), alpha),
-                                       __fmul_rn(__uint_as_float(v[c][4 * j + 1]), alpha),
-                                       __fmul_rn(__uint_as_float(v[c][4 * j + 2]), alpha),
-                                       __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
-              }
+              for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][e0 + e]), alpha));
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
+              const int c = 2 * ch + (j >> 2), e0 = 8 * (j & 3);  // columns 64 ch + 8 j .. + 7
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][e0 + 2 * e]), alpha),
+                                                         __fmul_rn(__uint_as_float(v[c][e0 + 2 * e + 1]), alpha));
+                w[e] = *reinterpret_cast<uint32_t*>(&b);
+              }
+            }
+            st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) * 16), w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
+          const int pc = lane & 7;
+          // this lane's first row (lane / 8) and its 16-byte piece of the chunk
+          constexpr int ESZ = F32 ? 4 : 2;
+          const int64_t pitch = p.ldd * ESZ;
+          uint8_t* dst = static_cast<uint8_t*>(p.d) +
+                         (static_cast<int64_t>(x.row0) + q * 32 + (lane >> 3)) * pitch +
+                         (static_cast<int64_t>(nt) * 128 + ch * CHUNK_COLS) * ESZ + pc * 16;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);                 // row within the warp's quarter
+            const uint4 d = ld_shared_v4(stg + rr * 128 + ((pc ^ (rr & 7)) * 16));
+            if (rr < rows_here) *reinterpret_cast<uint4*>(dst + 4 * i * pitch) = d;
+          }
+          __syncwarp();
+        }
+      } else {
+        if (!valid) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t col = static_cast<int64_t>(nt) * 128 + c * 32;
+          if constexpr (EPI == EPI_STORE_F32) {
+            float* drow = static_cast<float*>(p.d) + row * p.ldd + col;
+            if (p.d_align32) {
+              // whole 32-byte sectors per instruction
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                uint32_t w[4];
+                uint32_t o[8];
 #pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                  __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2]), alpha),
-                                                           __fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2 + 1]), alpha));
-                  w[h2] = *reinterpret_cast<uint32_t*>(&b);
-                }
-                dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 8; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[c][8 * j + e]), alpha));
+                st_global_v8(drow + 8 * j, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
               }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(drow);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__fmul_rn(__uint_as_float(v[c][4 * j]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 1]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 2]), alpha),
+                                     __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w[4];
+#pragma unroll
+              for (int h2 = 0; h2 < 4; ++h2) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2]), alpha),
+                                                         __fmul_rn(__uint_as_float(v[c][8 * j + 2 * h2 + 1]), alpha));
+                w[h2] = *reinterpret_cast<uint32_t*>(&b);
+              }
+              dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
         }
@@ -562,18 +641,27 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
 }
 
 template <int EPI, bool SMALL_A>
-cudaError_t launch_layout(const GemmArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch_layout(const GemmArgs& a, int grid, cudaStream_t s, const char** why) {
   auto k = grouped_gemm_kernel<EPI, SMALL_A>;
-  constexpr int bytes = Smem<SMALL_A>::BYTES;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  constexpr int bytes = Smem<SMALL_A, staged_store<EPI, SMALL_A>()>::BYTES;
+  // The register split assumes the block is launched with REG_LAUNCH registers a
+  // thread; with fewer, the epilogue's setmaxnreg.inc could never be granted.
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, k);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * THREADS < (REG_SF + REG_CTRL + 2 * REG_EPI) * 128 || fa.numRegs > REG_LAUNCH) {
+    *why = "the GEMM kernel was compiled with a register count its register split does not fit";
+    return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prefer_max_shared(reinterpret_cast<const void*>(k));
   return launch_kernel(k, dim3(grid), dim3(THREADS), bytes, s, a.pdl, a);
 }
 
 template <int EPI>
-cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s) {
-  return a.small_a ? launch_layout<EPI, true>(a, grid, s) : launch_layout<EPI, false>(a, grid, s);
+cudaError_t launch_epi(const GemmArgs& a, int grid, cudaStream_t s, const char** why) {
+  return a.small_a ? launch_layout<EPI, true>(a, grid, s, why) : launch_layout<EPI, false>(a, grid, s, why);
 }
 
 }  // namespace
@@ -586,9 +674,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** 
   if (grid > max_tiles) grid = static_cast<int>(max_tiles);
   if (grid < 1) grid = 1;
   switch (a.epilogue) {
-    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(a, grid, s);
-    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(a, grid, s);
-    case EPI_SWIGLU_QUANT: return launch_epi<EPI_SWIGLU_QUANT>(a, grid, s);
+    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(a, grid, s, why);
+    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(a, grid, s, why);
+    case EPI_SWIGLU_QUANT: return launch_epi<EPI_SWIGLU_QUANT>(a, grid, s, why);
     default: *why = "unknown epilogue"; return cudaErrorInvalidValue;
   }
 }

@@ -42,6 +42,11 @@ struct QuantArgs {
   uint8_t* codes;           // ROWMAJOR: [rows, K/2]; tiled layouts: the chunk buffer
   uint8_t* scales;          // ROWMAJOR: [rows, K/16]; unused otherwise
   int layout;               // OperandLayout
+  // Weight preparation (no device tables): without offsets, row p uses
+  // gs[p / rows_per_group] when rows_per_group > 0; with w13_I > 0 (and no
+  // gather) output row p reads input row w13_source_row(p, w13_I).
+  int32_t rows_per_group = 0;
+  int32_t w13_I = 0;
 };
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_global_scale(const void* x, int x_dtype, int64_t groups, int64_t n_per_group, float* gs_out,
@@ -73,8 +78,9 @@ size_t route_scratch_bytes(int32_t T, int32_t E);
 int route_kernel_launches(int32_t T, int32_t k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
-cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
-                           int32_t k, int32_t shared, int out_dtype, void* out, cudaStream_t s, bool pdl);
+// y [R, H] and out [T, H] of the same dtype (X_F32 or X_BF16).
+cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
+                           int32_t k, int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl);
 
 enum GemmEpilogue : int { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_SWIGLU_QUANT = 2 };
 

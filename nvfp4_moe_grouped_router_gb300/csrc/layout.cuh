@@ -16,7 +16,9 @@
 //   [16384, 18432)  four 512-byte scale atoms; atom kk covers K elements
 //                   64*kk .. 64*kk+63 of the K tile, and row r's 4 scales
 //                   (16 elements each) sit at (r % 32) * 16 + (r / 32) * 4 + b.
-//                   One tcgen05.cp 32x128b.warpx4 moves an atom into TMEM.
+//                   Four warps write an atom's 32 rows into TMEM with
+//                   tcgen05.st, one 32-lane quarter each (the layout the
+//                   block-scaled MMA reads its scale factors in).
 // Chunks are ordered tile-major: chunk (tile, kt) at (tile * nkt + kt) *
 // TILE_BYTES with nkt = ceil(K / 256).  The first 8*j rows of a chunk are its
 // first 1024*j bytes, so a partial tile can be loaded by a prefix copy.
@@ -47,6 +49,18 @@ __host__ __device__ __forceinline__ uint32_t tiled_code_offset(uint32_t r, uint3
   return r * 128u + ((((b >> 4) ^ (r & 7u)) << 4) | (b & 15u));
 }
 __host__ __device__ __forceinline__ int num_k_tiles(int K) { return (K + KT_ELEMS - 1) / KT_ELEMS; }
+
+// Prepared w13 row order: the fused SiLU-and-mul epilogue needs gate row i and
+// up row I + i in the same 32-row block.  Prepared row p of a stack of experts
+// (2I rows each) is canonical row w13_source_row(p, I) of the same stack:
+// within an expert, prepared rows [32c, 32c + 16) are gate rows [16c, 16c + 16)
+// and rows [32c + 16, 32c + 32) the up rows [I + 16c, I + 16c + 16).
+__host__ __device__ __forceinline__ int64_t w13_source_row(int64_t p, int32_t I) {
+  const int64_t e = p / (2 * I);
+  const int32_t r = static_cast<int32_t>(p - e * 2 * I);
+  const int32_t c = r >> 5, within = r & 31;
+  return e * 2 * I + (within < 16 ? 16 * c + within : I + 16 * c + within - 16);
+}
 
 // Largest g in [0, G) with offs[g] <= v (offs non-decreasing, offs[0] <= v < offs[G]).
 __device__ __forceinline__ int upper_group(const int32_t* offs, int G, int64_t v) {

@@ -64,8 +64,10 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t p = idx / gpr;
     const int gg = static_cast<int>(idx - p * gpr);
-    const int64_t src = a.gather ? static_cast<int64_t>(__ldg(a.gather + p)) : p;
-    const int g = grouped ? upper_group(offs, a.G, p) : 0;
+    const int64_t src = a.gather ? static_cast<int64_t>(__ldg(a.gather + p))
+                                 : (a.w13_I > 0 ? w13_source_row(p, a.w13_I) : p);
+    const int g = grouped ? upper_group(offs, a.G, p)
+                          : (a.rows_per_group > 0 ? static_cast<int>(p / a.rows_per_group) : 0);
     const float gs = __ldg(a.gs + g);
     float v[64];
     load64(a.x, a.x_dtype, src * a.ldx + gg * 64, v);

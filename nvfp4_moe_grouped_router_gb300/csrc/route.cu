@@ -374,17 +374,33 @@ __global__ void __launch_bounds__(kPermWarps * 32, 2) route_permute_kernel(Route
   }
 }
 
-// Eight consecutive outputs of one token per thread: one 256-bit load per slot
-// row (y rows are 32-byte aligned: 256-byte workspace, H % 128 == 0).  The
-// sum runs over the slots in order with one FMA per slot, then the shared row.
+// Eight consecutive outputs of one token per thread: one 256-bit (FP32 y) or
+// 128-bit (BF16 y) load per slot row (y rows are 32-byte aligned: 256-byte
+// workspace, H % 128 == 0).  The sum runs over the slots in order with one FMA
+// per slot in FP32, then the shared row.  y and out have the same type: FP32
+// for parity runs, BF16 for production (half the bytes of the y round trip).
 __device__ __forceinline__ void ld_nc_v8(const float* p, float (&v)[8]) {
   asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
                : "l"(p));
 }
+template <bool BF16>
+__device__ __forceinline__ void load_y8(const void* y, int64_t off, float (&v)[8]) {
+  if constexpr (BF16) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + off));
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      v[2 * c] = __uint_as_float(w4[c] << 16);
+      v[2 * c + 1] = __uint_as_float(w4[c] & 0xFFFF0000u);
+    }
+  } else {
+    ld_nc_v8(static_cast<const float*>(y) + off, v);
+  }
+}
 
-template <int OUT_BF16, bool BATCH>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int H, const float* __restrict__ w,
+template <bool BF16, bool BATCH>
+__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
                                                      void* out) {
   griddep_wait();
@@ -412,7 +428,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       float v[kCombineSlots][8];
 #pragma unroll
       for (int j = 0; j < kCombineSlots; ++j)
-        if (j < k) ld_nc_v8(y + row[j] + c * 8, v[j]);
+        if (j < k) load_y8<BF16>(y, row[j] + c * 8, v[j]);
 #pragma unroll
       for (int j = 0; j < kCombineSlots; ++j)
         if (j < k) {
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         const int64_t a = static_cast<int64_t>(t) * k + j;
         const float wj = __ldg(w + a);
         float v[8];
-        ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+        load_y8<BF16>(y, static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
       }
@@ -432,11 +448,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     if (shared) {
       const int64_t a = static_cast<int64_t>(T) * k + t;
       float v[8];
-      ld_nc_v8(y + static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+      load_y8<BF16>(y, static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
-    if (OUT_BF16) {
+    if constexpr (BF16) {
       uint32_t u[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -520,16 +536,16 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   return launch_route_nv<32>(a, s);
 }
 
-cudaError_t launch_combine(const float* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,
-                           int32_t shared, int out_dtype, void* out, cudaStream_t s, bool pdl) {
+cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,
+                           int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int64_t total = static_cast<int64_t>(T) * (H / 8);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
   if (blocks > cap) blocks = cap;
   const bool batch = T <= 256;
-  auto kern = out_dtype == X_BF16 ? (batch ? combine_kernel<1, true> : combine_kernel<1, false>)
-                                  : (batch ? combine_kernel<0, true> : combine_kernel<0, false>);
+  auto kern = dtype == X_BF16 ? (batch ? combine_kernel<true, true> : combine_kernel<true, false>)
+                              : (batch ? combine_kernel<false, true> : combine_kernel<false, false>);
   prefer_max_shared(reinterpret_cast<const void*>(kern));
   return launch_kernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, pdl, y, H, weights, s2p, T, k,
                        shared, out);

@@ -9,6 +9,7 @@
 
 namespace nvf {
 void set_last_error(const char* msg);
+nvf_status route_precheck(int32_t T, int32_t E, int32_t k, int32_t shared);
 }
 
 namespace {
@@ -47,8 +48,11 @@ extern "C" nvf_status moe_route_permute_noalloc(const float* logits, const float
                                                 int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
                                                 int32_t* tile_offsets, int32_t* perm_to_src, int32_t* src_to_perm,
                                                 int32_t* perm_token, void* stream) {
+  // Device and argument checks first, exactly as the workspace entry point makes them.
+  nvf_status st = nvf::route_precheck(T, E, k, shared_expert);
+  if (st != NVF_OK) return st;
   size_t need = 0;
-  nvf_status st = moe_route_permute_workspace_size(T, E, &need);
+  st = moe_route_permute_workspace_size(T, E, &need);
   if (st != NVF_OK) return st;
   if (need > kScratchBytes) {
     char msg[256];

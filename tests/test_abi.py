@@ -75,3 +75,16 @@ def test_compute_entry_points_fail_cleanly_without_a_gpu(nvf):
     st = L.nvfp4_quantize(None, 0, 0, 64, 64, None, None, None, 1, None, None, None, 0, None)
     assert st in (2, 4)   # unsupported device / CUDA error: no CPU fallback
     assert L.nvf_last_error_message()
+
+
+def test_route_entry_points_report_the_same_status_without_a_gpu(nvf):
+    """The no-alloc routing call makes the device check first, like the
+    workspace call: without a usable GB300 both return the same status and
+    neither touches its scratch."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    L = nvf.lib()
+    a = L.moe_route_permute(None, None, 16, 8, 2, 1, 0, None, None, None, None, None, None, None, None, 0, None)
+    b = L.moe_route_permute_noalloc(None, None, 16, 8, 2, 1, 0, None, None, None, None, None, None, None, None)
+    assert a == b and a in (2, 4)

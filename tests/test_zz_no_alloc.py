@@ -72,6 +72,55 @@ def test_matches_workspace_entry_point_on_consecutive_calls(nvf, first, second):
                 assert torch.equal(got[name], ref[name]), name
 
 
+def _scratch_need(nvf, T, E):
+    n = ctypes.c_size_t(0)
+    assert nvf.lib().moe_route_permute_workspace_size(T, E, ctypes.byref(n)) == 0
+    return n.value
+
+
+def test_largest_call_that_fits_matches_workspace_entry_point(nvf):
+    """T = 32736 tokens with 256 experts needs just under the 2 MiB of fixed
+    scratch (2 * 1023 * 256 + 256 words); it must run and agree with the
+    workspace entry point, twice in a row."""
+    T, E, k = 32736, 256, 8
+    need = _scratch_need(nvf, T, E)
+    assert need == (2 * 1023 * E + E) * 4 and (2 << 20) - 2048 < need <= (2 << 20)
+    g = torch.Generator().manual_seed(5)
+    logits = torch.randn(T, E, generator=g).cuda()
+    ref = _call(nvf, "moe_route_permute", logits, None, k, True, False)
+    for _ in range(2):
+        got = _call(nvf, "moe_route_permute_noalloc", logits, None, k, True, False)
+        for name in ref:
+            if name == "topk_w":
+                assert torch.allclose(got[name], ref[name], rtol=1e-6, atol=0), name
+            else:
+                assert torch.equal(got[name], ref[name]), name
+
+
+def test_smallest_call_that_does_not_fit_is_refused(nvf):
+    """One token more (a 1024th word column per expert) needs 2 MiB + 1 KB:
+    refused with NVF_ERR_WORKSPACE before anything is launched or written."""
+    T, E, k = 32737, 256, 8
+    assert _scratch_need(nvf, T, E) > (2 << 20)
+    logits = torch.zeros(T, E, device="cuda")
+    o = _outputs(T, E, k, False)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = nvf.lib().moe_route_permute_noalloc(p(logits), None, T, E, k, 1, 0, *[p(o[n]) for n in o], None)
+    assert st == 3, nvf.lib().nvf_last_error_message()
+    assert b"fixed" in nvf.lib().nvf_last_error_message()
+    torch.cuda.synchronize()
+    assert all(bool((v == -7).all()) for v in o.values())   # nothing was written
+
+
+def test_argument_errors_match_workspace_entry_point(nvf):
+    """A bad argument gets the status moe_route_permute returns (checked first)."""
+    L = nvf.lib()
+    for T, E, k in ((16, 8, 0), (16, 2000, 4), (-1, 8, 2)):
+        a = L.moe_route_permute(None, None, T, E, k, 1, 0, None, None, None, None, None, None, None, None, 0, None)
+        b = L.moe_route_permute_noalloc(None, None, T, E, k, 1, 0, None, None, None, None, None, None, None, None)
+        assert a == b == 1, (T, E, k, a, b)
+
+
 def test_rejects_sizes_beyond_the_fixed_scratch(nvf):
     T, E = 1 << 16, 1024
     n = ctypes.c_size_t(0)
