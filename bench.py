@@ -3,11 +3,16 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl ours|reference]
 
 A step is one pass of the whole layer (route, permute, quantize, gate_up GEMM
-with fused SiLU*up requant, down GEMM, combine) over one batch.  Default
-workload: the 30B-A3B-shaped decode layer (T=32, H=2048, I=768, E=128, top-8).
-Inputs are synthetic (seeded), weights are drawn on the device and prepared by
-the library before timing.  The timed region replays a CUDA graph of the K
-steps; the weights streamed per step (about 300 MB) exceed the 129 MB L2.
+with fused SiLU*up requant, down GEMM, combine; BF16 output) over one batch.
+Default workload: the 30B-A3B-shaped decode layer (T=32, H=2048, I=768, E=128,
+top-8), whose weight-streaming gate_up GEMM carries the headline roofline
+(fraction of HBM).  The same line carries a `prefill` object: the 4096-token
+prefill of the same layer (same weights), timed in the same process, with the
+grouped GEMMs' fraction of the dense FP4 tensor peak.  Inputs are synthetic
+(seeded: activations and logits from the CPU generator, weights drawn on the
+device and prepared by the library before timing).  The timed region replays a
+CUDA graph of the K steps; the weights streamed per step (about 300 MB) exceed
+the 129 MB L2.
 
 Multi-GPU: every rank runs its own replica on its own batch (the layer shards
 by tokens with no exchange): value = tokens of all ranks / max-over-ranks time.
@@ -26,6 +31,7 @@ import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
 import sys  # noqa: E402
+import tempfile  # noqa: E402
 import time  # noqa: E402
 
 import numpy as np  # noqa: E402
@@ -63,16 +69,25 @@ def activation_scales(name):
 
 
 def layer_bytes(cfg, counts):
-    """Algorithmic bytes of one step: weights of touched experts (codes + scales +
-    global scales), x, logits and out.  counts: rows per expert (shared included)."""
+    """Algorithmic bytes of one step (intermediates excluded): codes and block
+    scales of the touched experts' w13 and w2, their two FP32 global scales,
+    x (bf16), logits (fp32) and out (bf16).  counts: rows per expert (shared
+    included)."""
     touched = int((np.asarray(counts) > 0).sum())
     per_expert = 3 * cfg.H * cfg.I * (0.5 + 1.0 / 16) + 8
-    return touched, touched * per_expert + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.H * 4
+    return touched, touched * per_expert + cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4 + cfg.T * cfg.H * 2
 
 
-def gemm1_bytes(cfg, touched, R):
-    """Algorithmic bytes of the gate_up GEMM launch: w13 of touched experts, A1 in, A2 out."""
-    return touched * 2 * cfg.I * cfg.H * (0.5 + 1.0 / 16) + R * cfg.H * (0.5 + 1.0 / 16) + R * cfg.I * (0.5 + 1.0 / 16) / 2
+def gemm1_bytes(cfg, touched):
+    """Algorithmic bytes of the gate_up GEMM launch: codes, block scales and
+    global scale of the touched experts' w13 (the A1 / A2 intermediates are an
+    implementation cost, not counted)."""
+    return touched * (2 * cfg.I * cfg.H * (0.5 + 1.0 / 16) + 4)
+
+
+def gemm2_bytes(cfg, touched):
+    """Algorithmic bytes of the down GEMM launch: the touched experts' w2."""
+    return touched * (cfg.H * cfg.I * (0.5 + 1.0 / 16) + 4)
 
 
 class ClockSampler:
@@ -127,31 +142,82 @@ def oracle_sample(cfg, x, logits, bias, tokens, oracle_w):
                          np.full(E, gs1, np.float32), np.full(E, gs2, np.float32))
 
 
-def prepare_oracle_weights(cfg, x, logits, bias, tokens, seed):
+# ----------------------------------------------------------------------------- CPU oracle baseline
+# Each worker process holds its own copy of the layer's inputs and of the oracle's
+# quantized weights for the experts its token visits (drawn from the CPU
+# generator: the same recipe; the oracle's time does not depend on the values).
+_ORACLE = {}
+
+
+def _oracle_state(cfg_name, seed, token):
     from oracle import moe as M
-    ids, _ = M.route(logits[tokens].cpu().numpy(), None if bias is None else bias.cpu().numpy(), cfg.k,
-                     cfg.renormalize)
-    experts = sorted(set(ids.reshape(-1).tolist()) | ({cfg.E} if cfg.shared else set()))
-    out = {}
-    for e in experts:
-        w13, w2 = expert_weights(cfg, e, seed, device="cuda" if torch.cuda.is_available() else "cpu")
-        out[e] = (*M.quantize_expert_weights(w13.cpu().numpy()), *M.quantize_expert_weights(w2.cpu().numpy()))
-    return out
+    key = (cfg_name, seed)
+    if key not in _ORACLE:
+        cfg = CONFIGS[cfg_name]
+        x, logits, bias = make_inputs(cfg, seed, device="cpu")
+        _ORACLE[key] = (cfg, x, logits, bias, {})
+    cfg, x, logits, bias, ow = _ORACLE[key]
+    ids, _ = M.route(logits[[token]].numpy(), None if bias is None else bias.numpy(), cfg.k, cfg.renormalize)
+    for e in sorted(set(ids.reshape(-1).tolist()) | ({cfg.E} if cfg.shared else set())):
+        if e not in ow:
+            w13, w2 = expert_weights(cfg, e, seed, device="cpu")
+            ow[e] = (*M.quantize_expert_weights(w13.numpy()), *M.quantize_expert_weights(w2.numpy()))
+    return _ORACLE[key]
 
 
-def cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s):
-    """Tokens/s of the oracle (steps S1-S7, weights prepared beforehand) on a token sample."""
-    tokens = [0]
-    ow = prepare_oracle_weights(cfg, x, logits, bias, tokens, seed)
+def _oracle_job(args):
+    """One worker's share: (passes, seconds) of oracle forwards over one token
+    (steps S1-S7; weights prepared before the clock starts).  budget_s > 0: as
+    many passes as fit; budget_s == 0: set-up only; budget_s < 0: one pass."""
+    cfg_name, seed, token, budget_s = args
+    cfg, x, logits, bias, ow = _oracle_state(cfg_name, seed, token)
+    if budget_s == 0:
+        return 0, 0.0
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle_sample(cfg, x, logits, bias, tokens, ow)
+        oracle_sample(cfg, x, logits, bias, [token], ow)
         n += 1
         dt = time.perf_counter() - t0
-        if dt >= budget_s or n >= 1000:
-            break
-    return n * len(tokens) / dt, f"{n} oracle pass(es) over token 0 of the {cfg.name} batch ({len(ow)} experts)"
+        if budget_s < 0 or dt >= budget_s:
+            return n, dt
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    for line in open("/proc/cpuinfo"):
+        if line.startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    import platform
+    return platform.machine()
+
+
+def oracle_pool(cores):
+    import multiprocessing as mp
+    return mp.get_context("spawn").Pool(cores)
+
+
+def cpu_oracle_rates(cfg, seed, budget_s):
+    """Oracle tokens/s on one core (token 0) and on every core (one token per
+    core, tokens 0 .. cores-1), each worker single-threaded."""
+    cores = os.cpu_count() or 1
+    with oracle_pool(cores) as pool:
+        pool.map(_oracle_job, [(cfg.name, seed, t % cfg.T, 0) for t in range(cores)], chunksize=1)
+        n1, dt1 = pool.apply(_oracle_job, ((cfg.name, seed, 0, budget_s),))
+        res = pool.map(_oracle_job, [(cfg.name, seed, t % cfg.T, budget_s) for t in range(cores)], chunksize=1)
+    one = n1 / dt1
+    allc = sum(n / dt for n, dt in res)
+    sample = (f"oracle forwards (S1-S7) over single tokens of the {cfg.name} batch, weights prepared "
+              f"beforehand: token 0 on one core for {dt1:.1f} s ({n1} passes); tokens 0-{cores - 1}, "
+              f"one per core, for {budget_s:.0f} s ({sum(n for n, _ in res)} passes)")
+    return {"value": allc, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "one_core": one, "cpu_model": cpu_model()}
 
 
 def job_time_and_value(elapsed_ms, T, K, dist, device):
@@ -175,37 +241,36 @@ def workload_config(cfg, world):
 
 
 def run_reference(args, cfg):
+    """The reference arm: the CPU oracle as it stands, on every host core (one
+    token per core and step, each worker single-threaded; weights prepared
+    before timing).  A step is one oracle forward over `cores` tokens of the
+    workload; value = tokens / mean step time."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     seed = 0
-    x, logits, bias = make_inputs(cfg, seed, device="cpu")
-    total_budget = 150.0
-    per_step = max(1.0, total_budget / max(1, args.steps + args.warmup))
-    tokens = [0]
-    ow = prepare_oracle_weights(cfg, x, logits, bias, tokens, seed)
-    for _ in range(args.warmup):
-        oracle_sample(cfg, x, logits, bias, tokens, ow)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        n = 0
-        while True:
-            oracle_sample(cfg, x, logits, bias, tokens, ow)
-            n += 1
-            if time.perf_counter() - t0 >= per_step * 0.5 or n >= 50:
-                break
-        times.append((time.perf_counter() - t0) / n)
+    cores = os.cpu_count() or 1
+    jobs = [(cfg.name, seed, t % cfg.T, -1.0) for t in range(cores)]
+    with oracle_pool(cores) as pool:
+        pool.map(_oracle_job, [(n, s_, t, 0) for n, s_, t, _ in jobs], chunksize=1)   # set-up, untimed
+        for _ in range(args.warmup):
+            pool.map(_oracle_job, jobs, chunksize=1)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            pool.map(_oracle_job, jobs, chunksize=1)
+            times.append(time.perf_counter() - t0)
     ms = 1000 * statistics.mean(times)
-    value = len(tokens) / (ms / 1000)
-    cores = 1
+    value = cores / (ms / 1000)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": dict(workload_config(cfg, args.gpus), sample_tokens=len(tokens),
-                           timing="oracle on the host, wall clock, one token per sample"),
+            "config": dict(workload_config(cfg, args.gpus), sample_tokens=cores,
+                           timing="oracle on the host cores, wall clock; a step is one forward of "
+                                  f"{cores} tokens, one per core"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"token 0 of the {cfg.name} batch through the CPU oracle (S1-S7), one core"},
+                             "sample": f"tokens 0-{cores - 1} of the {cfg.name} batch through the CPU oracle "
+                                       "(S1-S7), one token per core per step", "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -318,162 +383,221 @@ def main():
     nvf.lib()
 
     seed = 0
-    x, logits, bias = make_inputs(cfg, seed + rank, device="cuda")
     w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, cfg.shared, lambda e: expert_weights(cfg, e, seed, device="cuda"))
-    gs1, gs2 = activation_scales(cfg.name)
-    gs_a1 = torch.full((cfg.E_total,), gs1, device="cuda")
-    gs_a2 = torch.full((cfg.E_total,), gs2, device="cuda")
-    ws = nvf.workspace(cfg.T, w, cfg.k)
-    out = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device="cuda")
-    cw = w.c_struct()
-
-    def step(events=None):
-        nvf.moe_forward(w, x, logits, cfg.k, gs_a1, gs_a2, bias=bias, renormalize=cfg.renormalize, out=out,
-                        ws=ws, stage_events=events, cw=cw)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    code, detail = nvf.device_status()
-    if code != 0:
-        raise RuntimeError(f"device error word {code} at {detail}")
     if args.profile:
-        for _ in range(args.steps):
-            step()
-        code, detail = nvf.device_status()
-        if code != 0:
-            raise RuntimeError(f"device error word {code} at {detail}")
+        run = LayerRun(nvf, cfg, w, seed + rank)
+        for _ in range(max(3, args.warmup) + args.steps):
+            run.step()
+        run.check()
         print(json.dumps({"profile_run": cfg.name, "steps": args.steps, "warmup": max(3, args.warmup),
                           "kernels_per_step": kernels_per_step(cfg.T)}))
         return
 
-    # --- graph of the K timed steps (kernels chained by programmatic dependent
-    # launch), and a second graph with an event at every stage boundary for the
-    # per-stage breakdown (events serialise the kernels, so it is timed apart).
-    K = args.steps
-    chunk = min(K, 256)
-    n_ev = 6
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(chunk)]
-    for row in ev:          # torch creates the CUDA event on first record
-        for e in row:
-            e.record()
-    torch.cuda.synchronize()
-    stream = torch.cuda.Stream()
-    stream.wait_stream(torch.cuda.current_stream())
-    graphs = []
-    with torch.cuda.stream(stream):
-        for n in sorted({chunk, K % chunk} - {0}, reverse=True):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    step()
-            graphs.append((n, g))
-        g_stages = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_stages, stream=stream):
-            for i in range(chunk):
-                step(ev[i])
-    torch.cuda.current_stream().wait_stream(stream)
-    plan = [graphs[0]] * (K // chunk) + ([g for g in graphs if g[0] == K % chunk] if K % chunk else [])
-    for n, g in graphs:    # warm the graphs
-        g.replay()
-    g_stages.replay()
-    torch.cuda.synchronize()
-
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    clocks = ClockSampler(os.path.join(out_dir, f"clocks_rank{rank}.csv") if os.path.isdir(out_dir)
-                          else f"/tmp/nvf_clocks_{os.getpid()}.csv")
-    clocks.start()
-    time.sleep(0.2)
-    # Soak (untimed): replay the same graph for ~1 s so that the clock samples
-    # taken around the (often millisecond-long) timed region see the load.
-    t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < 1.0:
-        plan[0][1].replay()
-        torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    start.record()
-    for n, g in plan:
-        g.replay()
-    end.record()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clk = clocks.stop()
-    elapsed_ms, value = job_time_and_value(start.elapsed_time(end), cfg.T, K, dist, "cuda")
-    code, detail = nvf.device_status()
-    if code != 0:
-        raise RuntimeError(f"device error word {code} at {detail}")
-
-    # per-stage durations from the event graph
-    g_stages.replay()
-    torch.cuda.synchronize()
-    stage_ms = {s: statistics.mean(ev[i][a].elapsed_time(ev[i][b]) for i in range(chunk)) for s, a, b in STAGES}
-    stage_step_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][5]) for i in range(chunk))
-
-    # --- end to end through the C ABI with host buffers
-    xh = x.cpu().pin_memory()
-    lh = logits.cpu().pin_memory()
-    oh = torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory()
-    xd, ld = torch.empty_like(x), torch.empty_like(logits)
-    Ke = min(K, 200)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(Ke):
-        xd.copy_(xh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
-        nvf.moe_forward(w, xd, ld, cfg.k, gs_a1, gs_a2, bias=bias, renormalize=cfg.renormalize, out=out, ws=ws,
-                        cw=cw)
-        oh.copy_(out, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    _, e2e_value = job_time_and_value(e0.elapsed_time(e1), cfg.T, Ke, dist, "cuda")
-
-    # --- roofline of the dominant kernel
-    L = nvf.workspace_layout(cfg.T, cfg.E, cfg.H, cfg.I, cfg.k, cfg.shared)
-    offs = ws[L["expert_offsets"]:L["expert_offsets"] + 4 * (cfg.E_total + 1)].view(torch.int32).cpu().numpy()
-    touched, lbytes = layer_bytes(cfg, np.diff(offs))
-    dominant = max(stage_ms, key=stage_ms.get)
     hbm, bf16, src = load_peaks()
-    R = cfg.R
-    g1 = gemm1_bytes(cfg, touched, R)
-    flops_g1 = 4.0 * R * cfg.H * cfg.I
-    fp4_peak_tflops = bf16 * 6.0           # dense FP4 / BF16 nominal ratio (13.5 / 2.25)
-    if dominant == "gate_up_gemm_swiglu_quant":
-        ach = g1 / (stage_ms[dominant] * 1e-3) / 1e9
-        roof = {"kernel": "grouped_gemm_kernel<SWIGLU_QUANT> (gate_up)", "bound": "hbm", "achieved": ach,
-                "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic_from_profiles(cfg.name),
-                "algorithmic_bytes": g1, "peak_source": src,
-                "tflops": flops_g1 / (stage_ms[dominant] * 1e-3) / 1e12,
-                "tc_frac_fp4": flops_g1 / (stage_ms[dominant] * 1e-3) / 1e12 / fp4_peak_tflops}
-    else:
-        roof = {"kernel": dominant, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
-                "traffic": None}
-
+    fp4_peak = bf16 * 6.0           # dense FP4 / BF16 nominal ratio (13.5 / 2.25), TFLOP/s
+    K = args.steps
+    run = LayerRun(nvf, cfg, w, seed + rank)
+    t = run.time(K, args.warmup, dist, rank, e2e=True)
+    elapsed_ms, value = job_time_and_value(t["elapsed_ms"], cfg.T, K, dist, "cuda")
+    _, e2e_value = job_time_and_value(t["e2e_ms"], cfg.T, t["e2e_steps"], dist, "cuda")
+    touched, lbytes = layer_bytes(cfg, t["counts"])
     ms_step = elapsed_ms / K
+    gemms = gemm_rooflines(cfg, t, touched, hbm, fp4_peak, src)
+    g1 = gemms["gate_up"]
+    roof = {"kernel": "grouped_gemm_kernel<SWIGLU_QUANT> (gate_up GEMM + SiLU*up + NVFP4 requant)",
+            "bound": "hbm", "achieved": g1["gbs"], "peak": hbm, "unit": "GB/s", "frac": g1["hbm_frac"],
+            "traffic": traffic_from_profiles(cfg.name), "algorithmic_bytes": g1["algorithmic_bytes"],
+            "duration_us": g1["us"], "peak_source": f"{src} HBM copy rate (burst)"}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales) -> f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, ue4m3 scales, fp32 accumulate) -> bf16",
+            "data": "synthetic",
             "config": dict(workload_config(cfg, world),
                            timing="CUDA graph of the K steps (programmatic dependent launch between kernels), "
                                   "CUDA events; stage_ms from a second graph with events at stage boundaries"),
-            "stage_ms": stage_ms, "stage_graph_ms_per_step": stage_step_ms,
+            "stage_ms": t["stage_ms"], "stage_graph_ms_per_step": t["stage_step_ms"],
             "layer_gbs": lbytes / (ms_step * 1e-3) / 1e9,
             "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
-            "roofline": roof, "clocks": clk, "gpu_launches": kernels_per_step(cfg.T) * K,
-            "e2e": {"value": e2e_value, "unit": "tokens/s",
-                    "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
-                    "d2h_bytes_per_step": out.numel() * 4}}
+            "gemms": gemms, "roofline": roof, "clocks": t["clocks"], "gpu_launches": kernels_per_step(cfg.T) * K,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": t["h2d"],
+                    "d2h_bytes_per_step": t["d2h"]}}
+    del run
+    if cfg.name == "decode" and world == 1:
+        line["prefill"] = prefill_object(nvf, w, seed + rank, min(K, 100), args.warmup, hbm, fp4_peak, src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample = cpu_oracle_rate(cfg, x, logits, bias, seed, budget_s=10.0)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_oracle_rates(cfg, seed, budget_s=10.0)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+class LayerRun:
+    """Device state of one workload: inputs (activations and logits from the CPU
+    generator, uploaded), activation scales, workspace and BF16 output."""
+
+    def __init__(self, nvf, cfg, w, seed):
+        self.nvf, self.cfg, self.w = nvf, cfg, w
+        x, logits, bias = make_inputs(cfg, seed, device="cpu")
+        self.x, self.logits = x.cuda(), logits.cuda()
+        self.bias = None if bias is None else bias.cuda()
+        gs1, gs2 = activation_scales(cfg.name)
+        self.gs_a1 = torch.full((cfg.E_total,), gs1, device="cuda")
+        self.gs_a2 = torch.full((cfg.E_total,), gs2, device="cuda")
+        self.ws = nvf.workspace(cfg.T, w, cfg.k)
+        self.out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+        self.cw = w.c_struct()
+
+    def step(self, events=None, x=None, logits=None):
+        c = self.cfg
+        self.nvf.moe_forward(self.w, self.x if x is None else x, self.logits if logits is None else logits, c.k,
+                             self.gs_a1, self.gs_a2, bias=self.bias, renormalize=c.renormalize, out=self.out,
+                             ws=self.ws, stage_events=events, cw=self.cw)
+
+    def check(self):
+        code, detail = self.nvf.device_status()
+        if code != 0:
+            raise RuntimeError(f"device error word {code} at {detail}")
+
+    def counts(self):
+        c = self.cfg
+        L = self.nvf.workspace_layout(c.T, c.E, c.H, c.I, c.k, c.shared)
+        o = L["expert_offsets"]
+        return np.diff(self.ws[o:o + 4 * (c.E_total + 1)].view(torch.int32).cpu().numpy())
+
+    def time(self, K, warmup, dist, rank, e2e=False):
+        """K steps replayed as CUDA graphs (kernels chained by programmatic
+        dependent launch), timed with CUDA events after a 1 s untimed soak,
+        clocks sampled around the timed region; per-stage times from a second
+        graph with an event at every stage boundary (events serialise the
+        kernels, so it is timed apart)."""
+        for _ in range(max(3, warmup)):
+            self.step()
+        torch.cuda.synchronize()
+        self.check()
+        chunk = min(K, 256)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(chunk)]
+        for row in ev:          # torch creates the CUDA event on first record
+            for e in row:
+                e.record()
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        graphs = []
+        with torch.cuda.stream(stream):
+            for n in sorted({chunk, K % chunk} - {0}, reverse=True):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(n):
+                        self.step()
+                graphs.append((n, g))
+            g_stages = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_stages, stream=stream):
+                for i in range(chunk):
+                    self.step(ev[i])
+        torch.cuda.current_stream().wait_stream(stream)
+        plan = [graphs[0]] * (K // chunk) + ([g for g in graphs if g[0] == K % chunk] if K % chunk else [])
+        for n, g in graphs:    # warm the graphs
+            g.replay()
+        g_stages.replay()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(os.path.join(tempfile.gettempdir(), f"nvf_clocks_{os.getpid()}_{rank}.csv"))
+        clocks.start()
+        time.sleep(0.2)
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 1.0:
+            plan[0][1].replay()
+            torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for n, g in plan:
+            g.replay()
+        end.record()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        res = {"elapsed_ms": start.elapsed_time(end), "clocks": clocks.stop()}
+        self.check()
+        g_stages.replay()
+        torch.cuda.synchronize()
+        res["stage_ms"] = {s: statistics.mean(ev[i][a].elapsed_time(ev[i][b]) for i in range(chunk))
+                           for s, a, b in STAGES}
+        res["stage_step_ms"] = statistics.mean(ev[i][0].elapsed_time(ev[i][5]) for i in range(chunk))
+        res["counts"] = self.counts()
+        if e2e:
+            # end to end through the C ABI with host buffers: H2D of x and logits
+            # from pinned memory, the layer, D2H of out, every step
+            xh, lh = self.x.cpu().pin_memory(), self.logits.cpu().pin_memory()
+            oh = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+            xd, ld = torch.empty_like(self.x), torch.empty_like(self.logits)
+            Ke = min(K, 200)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(Ke):
+                xd.copy_(xh, non_blocking=True)
+                ld.copy_(lh, non_blocking=True)
+                self.step(x=xd, logits=ld)
+                oh.copy_(self.out, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            self.check()
+            res.update(e2e_ms=e0.elapsed_time(e1), e2e_steps=Ke, h2d=self.x.numel() * 2 + self.logits.numel() * 4,
+                       d2h=self.out.numel() * 2)
+        return res
+
+
+def gemm_rooflines(cfg, t, touched, hbm, fp4_peak, src):
+    """Per-GEMM rates from the stage times: algorithmic bytes (weights of the
+    touched experts) and FLOPs, the fractions of the measured HBM copy rate and
+    of the dense FP4 tensor peak, and the fraction of the roofline time
+    max(FLOPs / FP4 peak, bytes / HBM rate)."""
+    R = cfg.R
+    out = {}
+    for name, stage, nbytes, flops in (
+            ("gate_up", "gate_up_gemm_swiglu_quant", gemm1_bytes(cfg, touched), 4.0 * R * cfg.H * cfg.I),
+            ("down", "down_gemm", gemm2_bytes(cfg, touched), 2.0 * R * cfg.H * cfg.I)):
+        sec = t["stage_ms"][stage] * 1e-3
+        t_hbm = nbytes / (hbm * 1e9)
+        t_tc = flops / (fp4_peak * 1e12)
+        out[name] = {"us": sec * 1e6, "algorithmic_bytes": nbytes, "flops": flops,
+                     "gbs": nbytes / sec / 1e9, "hbm_frac": nbytes / sec / 1e9 / hbm,
+                     "tflops": flops / sec / 1e12, "tc_frac_fp4": flops / sec / 1e12 / fp4_peak,
+                     "roofline_bound": "hbm" if t_hbm >= t_tc else "tensor",
+                     "roofline_us": max(t_hbm, t_tc) * 1e6, "roofline_frac": max(t_hbm, t_tc) / sec}
+    out["peaks"] = {"hbm_gbs": hbm, "fp4_tflops": fp4_peak,
+                    "source": f"{src}: HBM copy rate; FP4 = bf16 GEMM burst x 6 (nominal dense ratio 13.5 / 2.25)"}
+    return out
+
+
+def prefill_object(nvf, w, seed, K, warmup, hbm, fp4_peak, src):
+    """The prefill half of the metric: the same layer (same weights) at 4096
+    tokens, timed like the headline; the gate_up GEMM's fraction of the dense
+    FP4 tensor peak is its roofline."""
+    cfg = CONFIGS["prefill"]
+    run = LayerRun(nvf, cfg, w, seed)
+    t = run.time(K, warmup, None, 0)
+    ms = t["elapsed_ms"] / K
+    touched, lbytes = layer_bytes(cfg, t["counts"])
+    gemms = gemm_rooflines(cfg, t, touched, hbm, fp4_peak, src)
+    g1 = gemms["gate_up"]
+    obj = {"workload": workload_config(cfg, 1)["workload"], "T": cfg.T, "steps": K, "ms_per_step": ms,
+           "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "stage_ms": t["stage_ms"],
+           "stage_graph_ms_per_step": t["stage_step_ms"], "touched_experts": touched,
+           "layer_flops": 6.0 * cfg.R * cfg.H * cfg.I,
+           "layer_tflops": 6.0 * cfg.R * cfg.H * cfg.I / (ms * 1e-3) / 1e12,
+           "layer_gbs": lbytes / (ms * 1e-3) / 1e9, "gemms": gemms,
+           "roofline": {"kernel": "grouped_gemm_kernel<SWIGLU_QUANT> (gate_up)", "bound": "tensor",
+                        "achieved": g1["tflops"], "peak": fp4_peak, "unit": "TFLOP/s", "frac": g1["tc_frac_fp4"],
+                        "traffic": traffic_from_profiles(cfg.name), "roofline_bound": g1["roofline_bound"],
+                        "roofline_frac": g1["roofline_frac"], "duration_us": g1["us"],
+                        "peak_source": f"{src} bf16 GEMM burst x 6"},
+           "clocks": t["clocks"], "gpu_launches": kernels_per_step(cfg.T) * K}
+    del run
+    return obj
 
 
 def traffic_from_profiles(name):
