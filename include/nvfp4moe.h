@@ -32,22 +32,35 @@
  *            e4m3 * gs.  A block scale is E4M3(amax_block / (6 * gs)).
  * Operand layouts (enum nvf_layout):
  *   NVF_LAYOUT_ROWMAJOR      : codes uint8[rows][K/2], scales uint8[rows][K/16].
- *   NVF_LAYOUT_TILED         : one buffer of 18432-byte chunks, chunk (tile, kt)
- *                              at (tile * nkt + kt) * 18432, tile = row / 128,
- *                              nkt = ceil(K / 256).  A chunk holds K elements
- *                              [256 kt, 256 kt + 256) of 128 rows:
- *                              bytes [0, 16384): codes, 128 per row, code byte b
- *                                of row r at r*128 + (((b/16) ^ (r%8))*16) + b%16;
- *                              bytes [16384, 18432): four 512-byte scale atoms,
- *                                atom kk for K elements [64 kk, 64 kk + 64) of the
- *                                chunk, scale s (0..3) of row r at
- *                                (r%32)*16 + (r/32)*4 + s.
- *                              Size: nvfp4_tiled_bytes(rows, 0, K).
- *   NVF_LAYOUT_TILED_GROUPED : as TILED, but rows grouped by offsets[G+1]:
- *                              group g's rows form 128-row tiles numbered from
+ *   The tiled layouts cut a matrix into 128-row tiles and 256-element K tiles
+ *   (nkt = ceil(K / 256)); piece (tile, kt) holds K elements [256 kt, 256 kt + 256)
+ *   of 128 rows as
+ *     codes (16384 bytes): 128 per row, code byte b of row r at
+ *                          r*128 + (((b/16) ^ (r%8))*16) + b%16;
+ *     atoms (2048 bytes):  four 512-byte scale atoms, atom kk for K elements
+ *                          [64 kk, 64 kk + 64) of the piece, scale s (0..3) of
+ *                          row r at (r%32)*16 + (r/32)*4 + s.
+ *   NVF_LAYOUT_TILED_GROUPED : (activations) rows grouped by offsets[G+1]: group
+ *                              g's rows form 128-row tiles numbered from
  *                              tile_offsets[g] (exclusive prefix of
- *                              ceil(m_g / 128)).  Size: nvfp4_tiled_bytes(rows, G, K).
- *   Bytes of rows past a group's end, and of K past K in the last chunk, are
+ *                              ceil(m_g / 128)); piece (tile, kt) is the
+ *                              18432-byte chunk [codes][atoms] at
+ *                              (tile * nkt + kt) * 18432.
+ *                              Size: nvfp4_tiled_bytes(rows, G, K).
+ *   NVF_LAYOUT_TILED         : (weights) rows form G equal groups of R rows (one
+ *                              expert's N rows; G = 1 for a single matrix).
+ *                              Within a group, tiles 2p and 2p+1 form pair p,
+ *                              and K tile kt of pair p is one 36864-byte unit
+ *                              [codes 2p][codes 2p+1][atoms 2p][atoms 2p+1] at
+ *                              group_base + (2p*nkt + 2kt) * 18432; a group's
+ *                              last tile, when ceil(R/128) is odd, has
+ *                              18432-byte units [codes][atoms] at group_base +
+ *                              (2p*nkt + kt) * 18432.  group_base = g *
+ *                              ceil(R/128) * nkt * 18432.  A 256-column GEMM
+ *                              tile reads one unit per K tile with one copy.
+ *                              Size: nvfp4_tiled_bytes(rows, 0, K) (R a multiple
+ *                              of 128 when G > 1).
+ *   Bytes of rows past a group's end, and of K past K in the last K tile, are
  *   neither written nor read as data.
  *
  * Conventions.  All pointers marked "device" are device memory owned by the
@@ -123,7 +136,8 @@ nvf_status nvf_selftest_bounded_wait(uint64_t limit_ns, void* stream);
 nvf_status nvf_w13_row_map(int32_t I, int32_t* map);
 
 /* Bytes of a tiled operand buffer for up to `rows` rows, K columns and G
- * groups (G = 0: NVF_LAYOUT_TILED; G >= 1: NVF_LAYOUT_TILED_GROUPED). */
+ * groups (G = 0: NVF_LAYOUT_TILED, with groups of a multiple of 128 rows or one
+ * group; G >= 1: NVF_LAYOUT_TILED_GROUPED). */
 size_t nvfp4_tiled_bytes(int64_t rows, int32_t G, int32_t K);
 
 /* Per-group global scales gs[g] = amax(x[g]) / 2688 (1 when the group is all
@@ -140,8 +154,9 @@ nvf_status nvfp4_global_scale(const void* x, int32_t x_dtype, int64_t groups, in
  *                ldx * element size a multiple of 16.
  *   group_offsets device int32[G+1] (nullable): rows [offsets[g], offsets[g+1])
  *                use gscale[g]; required for NVF_LAYOUT_TILED_GROUPED together
- *                with tile_offsets (device int32[G+1]).  Without offsets
- *                gscale[0] is used for every row.
+ *                with tile_offsets (device int32[G+1]).  NVF_LAYOUT_TILED takes
+ *                no offsets: rows form G equal groups (rows % G == 0), group g
+ *                using gscale[g].  Otherwise gscale[0] is used for every row.
  *   gscale       device float (see above), finite and > 0.
  *   codes        device, 16-byte aligned: uint8[rows, K/2] for ROWMAJOR, the
  *                whole tiled buffer for the tiled layouts.
@@ -231,7 +246,7 @@ nvf_status moe_route_permute_noalloc(const float* logits, const float* bias, int
  *   D[row, n] = gs_a[g] * gs_b[g] * sum_k A[row, k] B[g*N + n, k]   for offsets[g] <= row < offsets[g+1].
  *   A       device NVF_LAYOUT_TILED_GROUPED buffer of K columns; a_rows bounds
  *           the rows (offsets[G] <= a_rows, buffer of nvfp4_tiled_bytes(a_rows, G, K)).
- *   B       device NVF_LAYOUT_TILED buffer of the [G*N, K] weight matrix.
+ *   B       device NVF_LAYOUT_TILED buffer of the [G*N, K] weight matrix (G groups of N rows).
  *   gs_a, gs_b device float[G]; group_offsets, tile_offsets device int32[G+1].
  *   N a positive multiple of 128, K a positive multiple of 64.
  *   D       device [a_rows, ldd] of out_dtype (NVF_F32 | NVF_BF16); only rows of
@@ -245,9 +260,9 @@ typedef struct nvf_moe_weights {
   int32_t E;               /* routed experts */
   int32_t H, I;            /* hidden, intermediate: multiples of 128 and 64 */
   int32_t shared;          /* 1: expert E is an always-on shared expert */
-  const uint8_t* w13;      /* NVF_LAYOUT_TILED [E'*2I, H], rows of each expert in nvf_w13_row_map order */
+  const uint8_t* w13;      /* NVF_LAYOUT_TILED [E'*2I, H] (groups of 2I rows), rows of each expert in nvf_w13_row_map order */
   const float* gs_w13;     /* float[E'] */
-  const uint8_t* w2;       /* NVF_LAYOUT_TILED [E'*H, I] */
+  const uint8_t* w2;       /* NVF_LAYOUT_TILED [E'*H, I] (groups of H rows) */
   const float* gs_w2;      /* float[E'] */
 } nvf_moe_weights;
 

@@ -144,15 +144,16 @@ def global_scale(x: torch.Tensor, groups: int = 1) -> torch.Tensor:
 
 
 def quantize(x: torch.Tensor, gscale: torch.Tensor, layout: int = LAYOUT_ROWMAJOR, gather=None, offsets=None,
-             tile_offsets=None, rows=None, codes=None, scales=None):
+             tile_offsets=None, rows=None, codes=None, scales=None, groups: int = 1):
     """NVFP4 quantization of the rows of a 2-D tensor x.
 
     ROWMAJOR: returns (codes [rows, K/2], scales [rows, K/16]); tiled layouts:
-    returns (buffer, None)."""
+    returns (buffer, None).  TILED (weights): rows form `groups` equal groups,
+    group g quantized with gscale[g]."""
     _cuda(x, "x")
     K = x.shape[1]
     rows = (gather.numel() if gather is not None else x.shape[0]) if rows is None else rows
-    G = offsets.numel() - 1 if offsets is not None else 1
+    G = offsets.numel() - 1 if offsets is not None else groups
     if codes is None:
         if layout == LAYOUT_ROWMAJOR:
             codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)

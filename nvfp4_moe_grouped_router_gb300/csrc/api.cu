@@ -266,6 +266,13 @@ nvf_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t rows, int32_t 
     NVF_REQUIRE(group_offsets && tile_offsets, "NVF_LAYOUT_TILED_GROUPED needs group_offsets and tile_offsets");
   QuantArgs a{x, x_dtype, rows, K, ldx, gather_rows, group_offsets, tile_offsets, group_offsets ? G : 1,
               gscale, codes, scales, layout};
+  if (layout == NVF_LAYOUT_TILED && group_offsets == nullptr) {
+    // weights: G equal groups of rows (one expert's N rows each), gscale[g] per group
+    NVF_REQUIRE(G >= 1 && rows % G == 0, "NVF_LAYOUT_TILED: rows=%lld must split into G=%d equal groups",
+                (long long)rows, G);
+    a.rows_per_group = rows > 0 ? static_cast<int32_t>(rows / G) : 0;
+    NVF_REQUIRE(rows / G < (int64_t(1) << 31), "group too large");
+  }
   NVF_CUDA(launch_quantize(a, static_cast<cudaStream_t>(stream)), "quantize launch");
   return NVF_OK;
 }

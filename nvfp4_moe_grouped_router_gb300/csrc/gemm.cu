@@ -20,23 +20,25 @@
 //
 // Roles (one CTA per SM, persistent, 512 threads = four warpgroups; setmaxnreg
 // gives the epilogue warpgroups 192 registers a thread, the others 64 and 56):
-//   warps 0-3   scale writers: as soon as a stage's scale atoms have landed
-//               (while its codes are still arriving), load them from shared
-//               memory and store them into the stage's TMEM scale slot (warp q
-//               writes lanes 32q..32q+31), then signal sf_ready.
+//   warps 0-3   scale writers: once a stage has landed, load its scale atoms
+//               from shared memory and store them into the stage's TMEM scale
+//               slot (warp q writes lanes 32q..32q+31), then signal sf_ready.
 //   warps 4-11  epilogue: two warps per 32-lane TMEM quarter, 128 columns
 //               each.  They move their whole slice of the accumulator to
 //               registers and release it before any arithmetic, so the next
 //               tile's MMAs run while this tile is finished: alpha and
 //               FP32/BF16 rows, or h = silu(gate) * up requantized to NVFP4
 //               straight into the next GEMM's tiled operand.
-//   warp 12     producer: per K tile the scale atoms of the A chunk and of the
-//               two B chunks of the tile's 256 weight rows (first, on their own
-//               barrier), then the A codes (valid-row prefix) and the B codes,
-//               moved with 1-D bulk copies into a 4- or 5-deep ring.  It issues
+//   warp 12     producer: per K tile the A chunk (one 18 KB copy of codes and
+//               atoms for a full tile; the valid-row prefix and the atoms
+//               otherwise) and the weight unit of the tile's 256 rows (one
+//               36 KB copy: the weight layout stores it as the stage holds
+//               it), moved with 1-D bulk copies into a 3- to 5-deep ring.  The
+//               ring's rate is set by the number of copies, not their bytes
+//               (measured: 54 KB stages as 6 copies stream 11.8 TB/s from L2,
+//               as 2 copies 17.4 TB/s), hence two copies a K tile.  It issues
 //               nothing else: L2 prefetches of the weights further ahead
-//               competed with the ring's own loads and cost the one issuing
-//               thread ~100+ cycles each, and measured slower at every depth.
+//               competed with the ring's own loads and measured slower.
 //   warp 13     MMA issuer: per K tile, once the codes have landed and the
 //               scales are in TMEM, four 128x256x64 MMAs into the single
 //               256-column TMEM accumulator.
@@ -101,7 +103,7 @@ struct Smem {
   static constexpr int STAGE_BYTES = ST_BSF + 2 * TILE_SF_BYTES;
   static constexpr int OFF_GRP = STAGES * STAGE_BYTES;  // int tile_offs[SMEM_GROUPS], offsets[SMEM_GROUPS]
   static constexpr int OFF_BAR = OFF_GRP + 2 * SMEM_GROUPS * 4 + 8;
-  static constexpr int NUM_BARS = 4 * STAGES + 3;  // full, empty, sf_full, sf_ready per stage; acc_full/empty, drain
+  static constexpr int NUM_BARS = 3 * STAGES + 3;  // full, empty, sf_ready per stage; acc_full/empty, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int STG_WARP_BYTES = 4096;        // 32 rows x 128 bytes
   static constexpr int OFF_STG = (OFF_MISC + 16 + 127) & ~127;
@@ -249,9 +251,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
   const uint32_t bar0 = s_base + OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
-  auto sfready_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };
-  const uint32_t accf_bar = bar0 + 8u * (4 * STAGES);
+  auto sfready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t accf_bar = bar0 + 8u * (3 * STAGES);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_mma_bar = accf_bar + 16u;
   auto stage_addr = [&](int s) { return s_base + static_cast<uint32_t>(s * STAGE_BYTES); };
@@ -263,7 +264,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-      mbar_init(sffull_bar(s), 1);
       mbar_init(sfready_bar(s), SF_WARPS);
     }
     mbar_init(accf_bar, 1);
@@ -294,9 +294,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       const Tile x = decode_tile(blockIdx.x, p, sc0);
       const int g = min(max(x.g, 0), p.G - 1);
       const int nt0 = min(max(x.nt0, 0), ntiles - (x.wide ? 2 : 1));
-      const uint8_t* bc = p.b + (static_cast<size_t>(g) * ntiles + nt0) * nkt * TILE_BYTES;
-      bulk_prefetch_l2(bc, static_cast<uint32_t>(nkt) * TILE_BYTES);
-      if (x.wide) bulk_prefetch_l2(bc + static_cast<size_t>(nkt) * TILE_BYTES, static_cast<uint32_t>(nkt) * TILE_BYTES);
+      // the tile's weight units, all K tiles: one contiguous range of the pair
+      const int pair = nt0 >> 1;
+      const uint8_t* bc = p.b + (static_cast<size_t>(g) * ntiles + 2 * pair) * nkt * TILE_BYTES;
+      bulk_prefetch_l2(bc, static_cast<uint32_t>((2 * pair + 1 < ntiles ? 2 : 1) * nkt) * TILE_BYTES);
     }
   }
   griddep_wait();
@@ -330,8 +331,16 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
           const Tile x = decode_tile(t, p, sc, gr);
           const uint8_t* a_chunk = p.a + static_cast<size_t>(x.mt) * nkt * TILE_BYTES;
-          const uint8_t* b_chunk = p.b + (static_cast<size_t>(x.g) * ntiles + x.nt0) * nkt * TILE_BYTES;
-          const int nbt = x.wide ? 2 : 1;
+          // Weights (TILED, groups of N rows): a 256-column tile reads one
+          // 36864-byte unit per K tile, [codes of both 128-row halves][their
+          // atoms], straight into the stage's [B codes][B atoms]; a 128-column
+          // tile reads its half's codes and atoms with two copies.
+          const int pair = x.nt0 >> 1, half = x.nt0 & 1;
+          const bool paired = 2 * pair + 1 < ntiles;
+          const uint8_t* b_pair = p.b + (static_cast<size_t>(x.g) * ntiles + 2 * pair) * nkt * TILE_BYTES;
+          const size_t b_unit = static_cast<size_t>(paired ? 2 : 1) * TILE_BYTES;
+          const size_t b_codes = paired ? static_cast<size_t>(half) * TILE_CODE_BYTES : 0;
+          const size_t b_atoms = paired ? 2 * TILE_CODE_BYTES + static_cast<size_t>(half) * TILE_SF_BYTES : TILE_CODE_BYTES;
           // rows of A to fetch: the valid ones, rounded up to the 8-row swizzle group
           int a_rows = x.rows;
           if (a_rows > SM::A_ROWS) {  // the caller promised at most 32 rows per group
@@ -339,25 +348,29 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             a_rows = SM::A_ROWS;
           }
           const uint32_t a_code_bytes = static_cast<uint32_t>((a_rows + 7) & ~7) * 128u;
+          const bool a_whole = !SMALL_A && a_rows == BM;    // codes and atoms in one copy
+          const uint32_t stage_tx = a_code_bytes + TILE_SF_BYTES + (x.wide ? 2 : 1) * TILE_BYTES;
           for (int kt = 0; kt < nkt; ++kt) {
             if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t)) {
               ok = false;
               break;
             }
             const uint32_t st = stage_addr(stage);
+            const uint32_t fb = full_bar(stage);
             const uint8_t* ac = a_chunk + static_cast<size_t>(kt) * TILE_BYTES;
-            // scale atoms first: the scale writers start on them while the codes arrive
-            mbar_arrive_expect_tx(sffull_bar(stage), (1 + nbt) * TILE_SF_BYTES);
-            bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
-            for (int h = 0; h < nbt; ++h) {
-              const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
-              bulk_load(st + ST_BSF + h * TILE_SF_BYTES, bc + TILE_CODE_BYTES, TILE_SF_BYTES, sffull_bar(stage));
+            const uint8_t* bu = b_pair + kt * b_unit;
+            mbar_arrive_expect_tx(fb, stage_tx);
+            if (a_whole) {
+              bulk_load(st + ST_A, ac, TILE_BYTES, fb);        // ST_ASF follows ST_A's 16 KB
+            } else {
+              bulk_load(st + ST_A, ac, a_code_bytes, fb);
+              bulk_load(st + ST_ASF, ac + TILE_CODE_BYTES, TILE_SF_BYTES, fb);
             }
-            mbar_arrive_expect_tx(full_bar(stage), a_code_bytes + nbt * TILE_CODE_BYTES);
-            bulk_load(st + ST_A, ac, a_code_bytes, full_bar(stage));
-            for (int h = 0; h < nbt; ++h) {
-              const uint8_t* bc = b_chunk + (static_cast<size_t>(h) * nkt + kt) * TILE_BYTES;
-              bulk_load(st + ST_B + h * TILE_CODE_BYTES, bc, TILE_CODE_BYTES, full_bar(stage));
+            if (x.wide) {
+              bulk_load(st + ST_B, bu, 2 * TILE_BYTES, fb);    // ST_BSF follows ST_B's 32 KB
+            } else {
+              bulk_load(st + ST_B, bu + b_codes, TILE_CODE_BYTES, fb);
+              bulk_load(st + ST_BSF, bu + b_atoms, TILE_SF_BYTES, fb);
             }
             pending |= 1u << stage;
             pend_par = (pend_par & ~(1u << stage)) | (ph << stage);
@@ -370,10 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         if (!ok || *abort_flag) {
           // Let every copy this thread issued land before the CTA goes away.
           for (int s = 0; s < STAGES; ++s)
-            if ((pending >> s) & 1u) {
-              mbar_wait_drain(sffull_bar(s), (pend_par >> s) & 1u, p.err, s);
-              mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
-            }
+            if ((pending >> s) & 1u) mbar_wait_drain(full_bar(s), (pend_par >> s) & 1u, p.err, s);
         }
       }
     } else if (warp == MMA_WARP) {
@@ -430,10 +440,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
       const Tile x = decode_tile(t, p, sc, gr);
       for (int kt = 0; kt < nkt; ++kt, ++i) {
         const int s = i % STAGES;
-        // The stage's atoms landed.  The MMAs of K tile i - STAGES, the last to
+        // The stage landed (atoms arrive with the codes).  The MMAs of K tile i - STAGES, the last to
         // read TMEM slot s, completed before the producer refilled the stage.
         // Every lane waits (and acquires); the warp leaves together if any lane gave up.
-        const bool got = mbar_wait(sffull_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
+        const bool got = mbar_wait(full_bar(s), (i / STAGES) & 1, abort_flag, p.err, DEV_TIMEOUT_PRODUCER, t);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;

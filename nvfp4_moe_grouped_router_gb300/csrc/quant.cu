@@ -75,15 +75,13 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     const uint32_t sf = quant_group64(v, gs, w);
     int64_t tile = 0;
     uint32_t r = 0;
-    if (a.layout == LAYOUT_TILED) {
-      tile = p >> 7;
-      r = static_cast<uint32_t>(p & 127);
-    } else if (a.layout == LAYOUT_TILED_GROUPED) {
+    if (a.layout == LAYOUT_TILED_GROUPED) {
       const int64_t local = p - offs[g];
       tile = toffs[g] + (local >> 7);
       r = static_cast<uint32_t>(local & 127);
     }
-    store_group64(a.codes, a.scales, a.layout, a.K, p, tile, r, gg, w, sf);
+    store_group64(a.codes, a.scales, a.layout, a.K, p, tile, r, gg, w, sf,
+                  a.rows_per_group > 0 ? a.rows_per_group : a.rows);
   }
 }
 

@@ -39,23 +39,34 @@ __device__ __forceinline__ uint32_t quant_group64(const float (&v)[64], float gs
 }
 
 // Store one quantized 64-element group (K elements 64*gg .. 64*gg+63) of row p.
-//   ROWMAJOR: codes/scales row-major.
-//   TILED*:   `tile` and `r` locate the row's 128-row tile; codes holds the chunks.
+//   ROWMAJOR:      codes/scales row-major.
+//   TILED_GROUPED: `tile` and `r` locate the row's 128-row tile; codes holds the chunks.
+//   TILED:         rows in groups of group_rows (weights); codes holds the units.
 __device__ __forceinline__ void store_group64(uint8_t* codes, uint8_t* scales, int layout, int K, int64_t p,
                                               int64_t tile, uint32_t r, int gg, const uint32_t (&w)[8],
-                                              uint32_t sf) {
+                                              uint32_t sf, int64_t group_rows = 0) {
   if (layout == LAYOUT_ROWMAJOR) {
     uint4* dst = reinterpret_cast<uint4*>(codes + p * (K / 2) + gg * 32);
     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     *reinterpret_cast<uint32_t*>(scales + p * (K / 16) + gg * 4) = sf;
-  } else {
-    uint8_t* chunk = codes + (static_cast<size_t>(tile) * num_k_tiles(K) + (gg >> 2)) * TILE_BYTES;
-    const uint32_t b = static_cast<uint32_t>(gg & 3) * 32u;
-    *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, b)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(chunk + tiled_code_offset(r, b + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
-    *reinterpret_cast<uint32_t*>(chunk + TILE_CODE_BYTES + (gg & 3) * 512 + sf_atom_offset(r, 0)) = sf;
+    return;
   }
+  uint8_t* cbase;
+  uint8_t* abase;
+  if (layout == LAYOUT_TILED) {
+    const TiledPos t = weight_tiled_pos(p, gg >> 2, group_rows, num_k_tiles(K));
+    cbase = codes + t.codes;
+    abase = codes + t.atoms;
+    r = t.r;
+  } else {
+    cbase = codes + (static_cast<size_t>(tile) * num_k_tiles(K) + (gg >> 2)) * TILE_BYTES;
+    abase = cbase + TILE_CODE_BYTES;
+  }
+  const uint32_t b = static_cast<uint32_t>(gg & 3) * 32u;
+  *reinterpret_cast<uint4*>(cbase + tiled_code_offset(r, b)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(cbase + tiled_code_offset(r, b + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+  *reinterpret_cast<uint32_t*>(abase + (gg & 3) * 512 + sf_atom_offset(r, 0)) = sf;
 }
 
 }  // namespace nvf

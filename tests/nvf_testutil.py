@@ -28,7 +28,7 @@ def atom_index(r128, b4):
 
 
 def row_tiles(rows: int, offsets=None, tile_offsets=None):
-    """(tile, r) of every row: TILED when offsets is None, else TILED_GROUPED."""
+    """(tile, r) of every row of a TILED_GROUPED operand (one group when offsets is None)."""
     p = np.arange(rows)
     if offsets is None:
         return p // 128, p % 128
@@ -40,7 +40,8 @@ def row_tiles(rows: int, offsets=None, tile_offsets=None):
 
 
 def tiled_index(tile, r, K):
-    """Byte offsets of every code byte [rows, K/2] and scale byte [rows, K/16]."""
+    """Byte offsets of every code byte [rows, K/2] and scale byte [rows, K/16] of a
+    TILED_GROUPED operand: 18432-byte chunk (tile, kt) = [codes][atoms]."""
     nkt = (K + 255) // 256
     tile = np.asarray(tile, dtype=np.int64)[:, None]
     r = np.asarray(r, dtype=np.int64)[:, None]
@@ -54,10 +55,54 @@ def tiled_index(tile, r, K):
 
 
 def tiled_unpack(buf, K, tile, r):
-    """Tiled operand bytes -> (codes [rows, K/2], scales [rows, K/16]) for rows at (tile, r)."""
+    """TILED_GROUPED bytes -> (codes [rows, K/2], scales [rows, K/16]) for rows at (tile, r)."""
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
     code, sf = tiled_index(tile, r, K)
     return buf[code], buf[sf]
+
+
+def weight_index(rows: int, K: int, group_rows: int):
+    """Byte offsets of every code byte [rows, K/2] and scale byte [rows, K/16] in
+    the TILED (weight) layout: groups of group_rows rows; within a group, tiles
+    2p and 2p + 1 share 36864-byte units [codes 2p][codes 2p+1][atoms 2p]
+    [atoms 2p+1] per K tile; an odd last tile has 18432-byte units."""
+    nkt = (K + 255) // 256
+    row = np.arange(rows, dtype=np.int64)
+    g, rl = row // group_rows, row % group_rows
+    ntg = (group_rows + 127) // 128
+    tile = rl // 128
+    pair, half = tile // 2, tile % 2
+    paired = 2 * pair + 1 < ntg
+    r = (rl % 128)[:, None]
+
+    def unit(kt):
+        return ((g * ntg + 2 * pair)[:, None] * nkt + kt * np.where(paired, 2, 1)[:, None]) * TILE_BYTES
+
+    b = np.arange(K // 2)[None, :]
+    kt, bb = b // 128, b % 128
+    codes = unit(kt) + np.where(paired, half * TILE_CODE_BYTES, 0)[:, None]
+    code = codes + r * 128 + (((bb // 16) ^ (r % 8)) * 16) + bb % 16
+    kb = np.arange(K // 16)[None, :]
+    kt2, kk, s = kb // 16, (kb % 16) // 4, kb % 4
+    atoms = unit(kt2) + np.where(paired, 2 * TILE_CODE_BYTES + half * 2048, TILE_CODE_BYTES)[:, None]
+    sf = atoms + kk * 512 + atom_index(r, s)
+    return code, sf
+
+
+def weight_unpack(buf, K, rows, group_rows):
+    """TILED (weight) bytes -> (codes [rows, K/2], scales [rows, K/16])."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    code, sf = weight_index(rows, K, group_rows)
+    return buf[code], buf[sf]
+
+
+def weight_pack(codes, scales, K, group_rows, nbytes):
+    """Inverse of weight_unpack; bytes not covered stay 0."""
+    out = np.zeros(nbytes, np.uint8)
+    code, sf = weight_index(codes.shape[0], K, group_rows)
+    out[code] = codes
+    out[sf] = scales
+    return out
 
 
 def tiled_pack(codes, scales, K, tile, r, nbytes):

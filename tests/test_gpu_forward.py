@@ -28,7 +28,7 @@ from oracle import moe as M
 from synth import CONFIGS, expert_weights, make_inputs
 from tests import oracle_pool
 from tests.nvf_testutil import (ROOT, dequant_check, ensure_built, quantize_rows_check, rel_err, row_tiles,
-                                 tiled_index, tiled_unpack, w13_prepared_rows)
+                                 tiled_unpack, w13_prepared_rows, weight_index)
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -224,8 +224,8 @@ def check_prepared_weights(nvf, layer, experts):
     cfg = layer.cfg
     n13, n2 = nvf.tiled_bytes(2 * cfg.I, 0, cfg.H), nvf.tiled_bytes(cfg.H, 0, cfg.I)
     perm = w13_prepared_rows(cfg.I)
-    i13 = [torch.from_numpy(a.astype(np.int64)).cuda() for a in tiled_index(*row_tiles(2 * cfg.I), cfg.H)]
-    i2 = [torch.from_numpy(a.astype(np.int64)).cuda() for a in tiled_index(*row_tiles(cfg.H), cfg.I)]
+    i13 = [torch.from_numpy(a.astype(np.int64)).cuda() for a in weight_index(2 * cfg.I, cfg.H, 2 * cfg.I)]
+    i2 = [torch.from_numpy(a.astype(np.int64)).cuda() for a in weight_index(cfg.H, cfg.I, cfg.H)]
     g13_all = layer.wts.gs_w13.cpu().numpy()
     g2_all = layer.wts.gs_w2.cpu().numpy()
     for e in experts:

@@ -11,7 +11,7 @@ import torch
 
 from oracle import formats as F
 from oracle import moe as M
-from tests.nvf_testutil import ensure_built, rel_err, row_tiles, tiled_pack
+from tests.nvf_testutil import ensure_built, rel_err, row_tiles, tiled_pack, weight_pack
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -38,9 +38,7 @@ def _run(nvf, a_codes, a_scales, sizes, w_codes, w_scales, gs_a, gs_w, out_dtype
     rows = max(R + pad_rows, 1)
     ta, ra = row_tiles(R, offs, tiles)
     A = tiled_pack(a_codes, a_scales, K, ta, ra, nvf.tiled_bytes(rows, G, K))
-    tb, rb = row_tiles(G * N)
-    B = tiled_pack(w_codes.reshape(G * N, Kh), w_scales.reshape(G * N, K // 16), K, tb, rb,
-                   nvf.tiled_bytes(G * N, 0, K))
+    B = weight_pack(w_codes.reshape(G * N, Kh), w_scales.reshape(G * N, K // 16), K, N, nvf.tiled_bytes(G * N, 0, K))
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     D = nvf.grouped_gemm(dev(A), rows, dev(B), dev(np.asarray(gs_a, np.float32)), dev(np.asarray(gs_w, np.float32)),
                          dev(offs.astype(np.int32)), dev(tiles.astype(np.int32)), N, K, out_dtype)

@@ -15,7 +15,7 @@ import torch
 
 from oracle import moe as M
 from synth import CONFIGS, expert_weights, make_inputs
-from tests.nvf_testutil import ensure_built, rel_err, row_tiles, tiled_unpack, w13_prepared_rows
+from tests.nvf_testutil import ensure_built, rel_err, w13_prepared_rows, weight_unpack
 
 pytestmark = pytest.mark.gpu
 TOL = 5e-3
@@ -70,9 +70,9 @@ def test_prepared_weights_equal_the_oracle(nvf, dtype):
     for e in range(cfg.E_total):
         c13, s13, g13 = M.quantize_expert_weights(w13_src[e].float().numpy())
         c2, s2, g2 = M.quantize_expert_weights(w2_src[e].float().numpy())
-        gc, gsc = tiled_unpack(w13[e * n13:(e + 1) * n13].cpu().numpy(), cfg.H, *row_tiles(2 * cfg.I))
+        gc, gsc = weight_unpack(w13[e * n13:(e + 1) * n13].cpu().numpy(), cfg.H, 2 * cfg.I, 2 * cfg.I)
         assert np.array_equal(gc, c13[perm]) and np.array_equal(gsc, s13[perm])
-        gc, gsc = tiled_unpack(w2[e * n2:(e + 1) * n2].cpu().numpy(), cfg.I, *row_tiles(cfg.H))
+        gc, gsc = weight_unpack(w2[e * n2:(e + 1) * n2].cpu().numpy(), cfg.I, cfg.H, cfg.H)
         assert np.array_equal(gc, c2) and np.array_equal(gsc, s2)
         assert gs13[e].item() == g13 and gs2[e].item() == g2
 
@@ -93,7 +93,7 @@ def test_zero_expert_gets_unit_scale(nvf):
     w13, gs13, w2, gs2 = _prepare(nvf, cfg, w13_src, w2_src, [cfg.E_total])
     assert gs13[2].item() == 1.0
     n13 = nvf.tiled_bytes(2 * cfg.I, 0, cfg.H)
-    gc, gsc = tiled_unpack(w13[2 * n13:3 * n13].cpu().numpy(), cfg.H, *row_tiles(2 * cfg.I))
+    gc, gsc = weight_unpack(w13[2 * n13:3 * n13].cpu().numpy(), cfg.H, 2 * cfg.I, 2 * cfg.I)
     assert not gc.any() and not gsc.any()
 
 

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from oracle import formats as F
-from tests.nvf_testutil import ensure_built, row_tiles, tiled_unpack
+from tests.nvf_testutil import ensure_built, row_tiles, tiled_unpack, weight_unpack
 
 pytestmark = pytest.mark.gpu
 
@@ -62,26 +62,38 @@ def test_ties_signed_zero_and_saturation(nvf):
     _check_rowmajor(nvf, x.to(torch.bfloat16), np.float32(1.0))
 
 
-@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("groups,group_rows", [(1, 517), (3, 384), (2, 512)])
 @pytest.mark.parametrize("K", [512, 320, 64])
-def test_tiled_layouts(nvf, layout, K):
+def test_weight_layout(nvf, groups, group_rows, K):
+    """TILED (weights): groups of rows with one global scale each; paired
+    36864-byte units, and an odd last tile per group (517 and 384 rows)."""
+    rows = groups * group_rows
+    x = torch.randn(rows, K, generator=torch.Generator().manual_seed(3 + groups)).to(torch.bfloat16)
+    gs = np.array([F.global_scale(float(x[g * group_rows:(g + 1) * group_rows].float().abs().max()))
+                   for g in range(groups)], np.float32)
+    ref_c, ref_s = F.quantize_rows(x.float().numpy(), np.repeat(gs, group_rows))
+    buf, _ = nvf.quantize(x.cuda(), torch.tensor(gs, device="cuda"), layout=1, groups=groups)
+    c, s_ = weight_unpack(buf.cpu().numpy(), K, rows, group_rows)
+    assert np.array_equal(c, ref_c)
+    assert np.array_equal(s_, ref_s)
+
+
+@pytest.mark.parametrize("K", [512, 320, 64])
+def test_grouped_activation_layout(nvf, K):
+    """TILED_GROUPED (activations): per-group 128-row tiles, empty groups included."""
     rows = 517
     x = torch.randn(rows, K, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
     gs = F.global_scale(float(x.float().abs().max()))
     ref_c, ref_s = F.quantize_rows(x.float().numpy(), gs)
-    if layout == 1:
-        buf, _ = _gpu_quant(nvf, x.cuda(), gs, layout=1)
-        tile, r = row_tiles(rows)
-    else:
-        sizes = np.array([0, 130, 1, 0, 256, 127, 3], np.int64)
-        sizes[-1] = rows - sizes[:-1].sum()
-        offs = np.concatenate([[0], np.cumsum(sizes)])
-        tiles = np.concatenate([[0], np.cumsum((sizes + 127) // 128)])
-        gsv = torch.full((len(sizes),), float(gs), dtype=torch.float32, device="cuda")
-        buf, _ = _gpu_quant(nvf, x.cuda(), gsv, layout=2,
-                            offsets=torch.tensor(offs, dtype=torch.int32, device="cuda"),
-                            tile_offsets=torch.tensor(tiles, dtype=torch.int32, device="cuda"))
-        tile, r = row_tiles(rows, offs, tiles)
+    sizes = np.array([0, 130, 1, 0, 256, 127, 3], np.int64)
+    sizes[-1] = rows - sizes[:-1].sum()
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    tiles = np.concatenate([[0], np.cumsum((sizes + 127) // 128)])
+    gsv = torch.full((len(sizes),), float(gs), dtype=torch.float32, device="cuda")
+    buf, _ = _gpu_quant(nvf, x.cuda(), gsv, layout=2,
+                        offsets=torch.tensor(offs, dtype=torch.int32, device="cuda"),
+                        tile_offsets=torch.tensor(tiles, dtype=torch.int32, device="cuda"))
+    tile, r = row_tiles(rows, offs, tiles)
     c, s_ = tiled_unpack(buf, K, tile, r)
     assert np.array_equal(c, ref_c)
     assert np.array_equal(s_, ref_s)
