@@ -46,7 +46,7 @@ namespace {
 constexpr int kMaxE = 1024;          // routed experts
 constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
 constexpr int kPermWarps = 16;       // tokens per permute CTA
-constexpr int kCombineSlots = 10;    // the combine keeps up to this many slots in flight per thread
+constexpr int kCombineSlots = 8;     // the combine keeps up to this many slots in flight per thread
 
 template <int NV>
 constexpr int topk_threads() { return NV <= 8 ? 1024 : 512; }
@@ -384,88 +384,100 @@ __device__ __forceinline__ void ld_nc_v8(const float* p, float (&v)[8]) {
                : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
                : "l"(p));
 }
+// Raw y of 8 consecutive outputs: 16 bytes (BF16) or 32 bytes (FP32).
 template <bool BF16>
-__device__ __forceinline__ void load_y8(const void* y, int64_t off, float (&v)[8]) {
+struct Y8 {
+  uint32_t w[BF16 ? 4 : 8];
+};
+template <bool BF16>
+__device__ __forceinline__ Y8<BF16> load_y8_raw(const void* y, int64_t off) {
+  Y8<BF16> r;
   if constexpr (BF16) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + off));
-    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      v[2 * c] = __uint_as_float(w4[c] << 16);
-      v[2 * c + 1] = __uint_as_float(w4[c] & 0xFFFF0000u);
-    }
+    r.w[0] = u.x; r.w[1] = u.y; r.w[2] = u.z; r.w[3] = u.w;
   } else {
+    float v[8];
     ld_nc_v8(static_cast<const float*>(y) + off, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r.w[e] = __float_as_uint(v[e]);
   }
+  return r;
+}
+template <bool BF16>
+__device__ __forceinline__ float y8_at(const Y8<BF16>& r, int e) {
+  if constexpr (BF16) return __uint_as_float((e & 1) ? (r.w[e >> 1] & 0xFFFF0000u) : (r.w[e >> 1] << 16));
+  else return __uint_as_float(r.w[e]);
 }
 
-template <bool BF16, bool BATCH>
-__global__ void __launch_bounds__(256) combine_kernel(const void* __restrict__ y, int H, const float* __restrict__ w,
+// One thread per 8 consecutive outputs of one token (grid covers every output
+// once).  The token's slot rows and routing weights come from the routing
+// kernel, three launches back, which is complete before this kernel may begin
+// (the down GEMM it follows waited on the gate_up GEMM, which waited on the
+// routing): they are loaded before the dependency wait, and only the y rows
+// after it, all slots at once.
+template <bool BF16>
+__global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
                                                      void* out) {
-  griddep_wait();
   const int h8 = H >> 3;
-  const int64_t total = static_cast<int64_t>(T) * h8;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(idx / h8);
-    const int c = static_cast<int>(idx - static_cast<int64_t>(t) * h8);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (BATCH && k <= kCombineSlots) {
-      // Few tokens (latency-bound): all slot rows and weights first, then all
-      // row loads -- two round trips of memory latency instead of two per slot.
-      // Many tokens keep the plain loop: its lower register count keeps more
-      // threads resident, which a bandwidth-bound pass needs more.
-      int64_t row[kCombineSlots];
-      float wv[kCombineSlots];
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const bool live = idx < static_cast<int64_t>(T) * h8;
+  const int t = live ? static_cast<int>(idx / h8) : 0;
+  const int c = live ? static_cast<int>(idx - static_cast<int64_t>(t) * h8) : 0;
+  const int kb = min(k, kCombineSlots);
+  int64_t row[kCombineSlots];
+  float wv[kCombineSlots];
+  int64_t srow = 0;
+  if (live) {
 #pragma unroll
-      for (int j = 0; j < kCombineSlots; ++j)
-        if (j < k) {
-          const int64_t a = static_cast<int64_t>(t) * k + j;
-          wv[j] = __ldg(w + a);
-          row[j] = static_cast<int64_t>(__ldg(s2p + a)) * H;
-        }
-      float v[kCombineSlots][8];
-#pragma unroll
-      for (int j = 0; j < kCombineSlots; ++j)
-        if (j < k) load_y8<BF16>(y, row[j] + c * 8, v[j]);
-#pragma unroll
-      for (int j = 0; j < kCombineSlots; ++j)
-        if (j < k) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[j], v[j][e], acc[e]);
-        }
-    } else {
-      for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < kCombineSlots; ++j)
+      if (j < kb) {
         const int64_t a = static_cast<int64_t>(t) * k + j;
-        const float wj = __ldg(w + a);
-        float v[8];
-        load_y8<BF16>(y, static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, v[e], acc[e]);
+        wv[j] = __ldg(w + a);
+        row[j] = static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8;
       }
-    }
-    if (shared) {
-      const int64_t a = static_cast<int64_t>(T) * k + t;
-      float v[8];
-      load_y8<BF16>(y, static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8, v);
+    if (shared) srow = static_cast<int64_t>(__ldg(s2p + static_cast<int64_t>(T) * k + t)) * H + c * 8;
+  }
+  griddep_wait();
+  if (!live) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  {
+    Y8<BF16> v[kCombineSlots];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += v[e];
-    }
-    if constexpr (BF16) {
-      uint32_t u[4];
+    for (int j = 0; j < kCombineSlots; ++j)
+      if (j < kb) v[j] = load_y8_raw<BF16>(y, row[j]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
-        u[e] = *reinterpret_cast<uint32_t*>(&b);
+    for (int j = 0; j < kCombineSlots; ++j)
+      if (j < kb) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wv[j], y8_at<BF16>(v[j], e), acc[e]);
       }
-      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(t) * H)[c] =
-          make_uint4(u[0], u[1], u[2], u[3]);
-    } else {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * H) + 2 * c;
-      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  for (int j = kCombineSlots; j < k; ++j) {   // more than kCombineSlots slots: the rest one at a time
+    const int64_t a = static_cast<int64_t>(t) * k + j;
+    const float wj = __ldg(w + a);
+    const Y8<BF16> v = load_y8_raw<BF16>(y, static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj, y8_at<BF16>(v, e), acc[e]);
+  }
+  if (shared) {
+    const Y8<BF16> v = load_y8_raw<BF16>(y, srow);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += y8_at<BF16>(v, e);
+  }
+  if constexpr (BF16) {
+    uint32_t u[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+      u[e] = *reinterpret_cast<uint32_t*>(&b);
     }
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(t) * H)[c] =
+        make_uint4(u[0], u[1], u[2], u[3]);
+  } else {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + static_cast<int64_t>(t) * H) + 2 * c;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
@@ -540,12 +552,8 @@ cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const
                            int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
   const int64_t total = static_cast<int64_t>(T) * (H / 8);
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
-  if (blocks > cap) blocks = cap;
-  const bool batch = T <= 256;
-  auto kern = dtype == X_BF16 ? (batch ? combine_kernel<true, true> : combine_kernel<true, false>)
-                              : (batch ? combine_kernel<false, true> : combine_kernel<false, false>);
+  const int64_t blocks = (total + 255) / 256;   // one output group per thread (T <= 2^24, H <= 2^20: fits the grid)
+  auto kern = dtype == X_BF16 ? combine_kernel<true> : combine_kernel<false>;
   prefer_max_shared(reinterpret_cast<const void*>(kern));
   return launch_kernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, pdl, y, H, weights, s2p, T, k,
                        shared, out);
