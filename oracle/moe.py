@@ -38,6 +38,30 @@ F32 = np.float32
 TILE_M = 128
 
 
+# ----------------------------------------------------------------------------- router gate
+def router_logits(x, w_gate):
+    """Router gate, the step before routing: logits[t, j] = sum_h x[t, h] *
+    w_gate[j, h] for bf16 activations x [T, H] and bf16 gate rows w_gate
+    [n, H] (given here as their exact float values).  Every product of two bf16
+    values is exact in float64 and the sum is taken in float64, then rounded
+    once to float32 (the logits' type).  The pages name the routed experts the
+    gate scores (FlashInfer issue #2723, "Model" table: 512 routed + 1 shared,
+    10 per token) but give no gate formula; reading: a plain linear gate
+    without bias, one row per routed expert, plus optionally one row whose
+    logit gates the shared expert (shared_gate)."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_gate, dtype=np.float64)
+    return (x @ w.T).astype(F32)
+
+
+def shared_gate(gate_logit):
+    """Weight of the shared expert's output: sigmoid of its gate logit, float64.
+    Reading (the pages give no formula): sigmoid(z) = 1 / (1 + exp(-z))."""
+    z = np.asarray(gate_logit, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
 # ----------------------------------------------------------------------------- routing
 def route(logits, bias, k: int, renormalize: bool = True):
     """Top-k selection and softmax weights.
@@ -139,8 +163,9 @@ def swiglu(c1, I: int) -> np.ndarray:
         return g / (1.0 + np.exp(-g)) * u
 
 
-def combine(y, weights, src_to_perm, T: int, k: int, shared: bool):
-    """out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ y of the shared row), float64."""
+def combine(y, weights, src_to_perm, T: int, k: int, shared: bool, shared_weight=None):
+    """out[t] = sum_j w[t,j] * y[src_to_perm[t*k+j]] (+ g[t] * y of the shared row), float64.
+    g[t] = 1 without a shared-expert gate, else shared_weight[t]."""
     y = np.asarray(y, dtype=np.float64)
     w = np.asarray(weights, dtype=np.float64)
     rows = np.asarray(src_to_perm[: T * k]).reshape(T, k)
@@ -148,7 +173,8 @@ def combine(y, weights, src_to_perm, T: int, k: int, shared: bool):
     for j in range(k):                       # slot order
         out += w[:, j:j + 1] * y[rows[:, j]]
     if shared:
-        out += y[np.asarray(src_to_perm[T * k: T * k + T])]
+        ys = y[np.asarray(src_to_perm[T * k: T * k + T])]
+        out += ys if shared_weight is None else np.asarray(shared_weight, np.float64)[:, None] * ys
     return out
 
 
@@ -162,7 +188,7 @@ def quantize_expert_weights(w_fp32):
 
 
 # ----------------------------------------------------------------------------- layer
-def moe_forward(x, logits, bias, k, renormalize, shared, weights, gs_a1, gs_a2, experts=None):
+def moe_forward(x, logits, bias, k, renormalize, shared, weights, gs_a1, gs_a2, experts=None, shared_gate_logit=None):
     """Whole layer, returning every intermediate.
 
     x        : float32 [T, H] (the bf16 activations, exactly converted)
@@ -171,6 +197,8 @@ def moe_forward(x, logits, bias, k, renormalize, shared, weights, gs_a1, gs_a2, 
     gs_a1/2  : float32 [E'] static activation global scales
     experts  : optional set of experts to evaluate; rows of other experts are
                left as NaN (for sampled checks of large layers).
+    shared_gate_logit : optional float32 [T]: the shared expert's output is
+               scaled by shared_gate(logit) instead of 1.
     """
     x = np.asarray(x, dtype=F32)
     T, H = x.shape
@@ -207,5 +235,6 @@ def moe_forward(x, logits, bias, k, renormalize, shared, weights, gs_a1, gs_a2, 
         a2_codes[lo:hi], a2_scales[lo:hi] = qc, qs
         y[lo:hi] = np.float64(alpha(gs_a2[e], gw2)) * block_scaled_matmul(qc, qs, w2c, w2s)
     out.update(c1=c1, h=h, a2_codes=a2_codes, a2_scales=a2_scales, y=y)
-    out["out"] = combine(y, w, s2p, T, k, shared) if y is not None else None
+    sw = None if shared_gate_logit is None else shared_gate(shared_gate_logit)
+    out["out"] = combine(y, w, s2p, T, k, shared, sw) if y is not None else None
     return out

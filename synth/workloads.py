@@ -70,7 +70,7 @@ CONFIGS = {
                           description="Zipf(1.2)-biased routing stress, 8192 tokens"),
 }
 
-_STREAM_X, _STREAM_LOGITS, _STREAM_W13, _STREAM_W2 = 1, 2, 3, 4
+_STREAM_X, _STREAM_LOGITS, _STREAM_W13, _STREAM_W2, _STREAM_GATE = 1, 2, 3, 4, 5
 
 
 def _seed(seed: int, stream: int, index: int = 0) -> int:
@@ -105,3 +105,13 @@ def expert_weights(cfg: LayerConfig, e: int, seed: int = 0, device="cpu"):
     w2 = torch.randn(cfg.H, cfg.I, generator=_gen(device, seed, _STREAM_W2, e), device=device,
                      dtype=torch.float32) * 0.02
     return w13, w2
+
+
+def gate_weights(cfg: LayerConfig, seed: int = 0, shared_gate: bool = False, device="cpu"):
+    """Router gate rows, bf16 [E (+1), H]: 0.02 * N(0, 1) drawn in FP32 and rounded
+    to bf16 (so x . w_gate has a spread like the N(0, 1) logits of the recipe);
+    with shared_gate, one more row that gates the shared expert."""
+    n = cfg.E + (1 if shared_gate else 0)
+    w = torch.randn(n, cfg.H, generator=_gen(device, seed, _STREAM_GATE), device=device,
+                    dtype=torch.float32) * 0.02
+    return w.to(torch.bfloat16)
