@@ -276,6 +276,7 @@ typedef struct nvf_moe_ws_layout {
   size_t a2;                /* NVF_LAYOUT_TILED_GROUPED, K = I */
   size_t y;                 /* [R, H], row = permuted slot: float when the forward's out is NVF_F32, bf16
                                when it is NVF_BF16 (the region is sized for float) */
+  size_t logits;            /* float[T, E + gated]: the router gate's output (nvfp4_moe_forward_gated only) */
   size_t total;
   int64_t R;                /* rows after permutation */
 } nvf_moe_ws_layout;
@@ -304,6 +305,32 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
                              int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,
                              int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
                              void* const* stage_events, void* stream);
+
+/* Router gate, the step before routing: logits[t * ldl + j] = sum_h x[t, h] *
+ * w_gate[j, h] for j < n, with BF16 inputs multiplied on the tensor cores and
+ * summed in FP32.
+ *   x       device bf16 [T, H] (row pitch H), 16-byte aligned; H a positive
+ *           multiple of 64.
+ *   w_gate  device bf16 [n, H]: one row per routed expert, plus, for a gated
+ *           shared expert, one more row whose logit gates it.
+ *   logits  device float [T, ldl], ldl >= n; columns j < n are written.
+ * The pages name the experts the gate scores (FlashInfer issue #2723, "Model"
+ * table: 512 routed + 1 shared expert, 10 routed per token) but give no gate
+ * formula: this is the plain linear gate without bias.  Asynchronous on
+ * `stream`; a bounded wait that expires is reported through nvf_device_status. */
+nvf_status nvf_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t H, int32_t n, float* logits,
+                           int64_t ldl, void* stream);
+
+/* The layer from the hidden states: the router gate (nvf_router_gemm with
+ * w_gate bf16 [E + shared_gate, H], logits into the workspace's `logits`
+ * region), then steps 1-7 as nvfp4_moe_forward.  shared_gate = 1 (the layer
+ * must have a shared expert) scales the shared expert's output by
+ * sigmoid(x . w_gate[E]) instead of 1 (the reading of a gated shared expert;
+ * the pages give no formula).  Other arguments as nvfp4_moe_forward. */
+nvf_status nvfp4_moe_forward_gated(const nvf_moe_weights* w, const void* w_gate, int32_t shared_gate, const void* x,
+                                   const float* bias, int32_t T, int32_t k, int32_t renormalize, const float* gs_a1,
+                                   const float* gs_a2, int32_t out_dtype, void* out, void* ws, size_t ws_bytes,
+                                   void* stream);
 
 #ifdef __cplusplus
 }

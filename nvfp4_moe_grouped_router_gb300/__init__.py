@@ -44,6 +44,9 @@ SIGNATURES = {
                                                  _P]),
     "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
                                          _P]),
+    "nvf_router_gemm": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P]),
+    "nvfp4_moe_forward_gated": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ,
+                                               _P]),
 }
 
 
@@ -61,7 +64,7 @@ class MoEWeightsC(ctypes.Structure):
 class WorkspaceLayoutC(ctypes.Structure):
     _fields_ = [(n, _SZ) for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src",
                                     "src_to_perm", "perm_token", "route_scratch", "tile_group", "a1", "a2", "y",
-                                    "total")] + [("R", _I64)]
+                                    "logits", "total")] + [("R", _I64)]
 
 
 _lib = None
@@ -280,4 +283,37 @@ def moe_forward(w: MoEWeights, x, logits, k: int, gs_a1, gs_a2, bias=None, renor
     _check(lib().nvfp4_moe_forward(ctypes.byref(cw), _ptr(x), _ptr(logits), _ptr(bias), T, k, int(renormalize),
                                    _ptr(gs_a1), _ptr(gs_a2), NVF_F32 if out.dtype == torch.float32 else NVF_BF16,
                                    _ptr(out), _ptr(h_dump), _ptr(ws), ws.numel(), ev, _stream()))
+    return out
+
+
+def router_gemm(x, w_gate, logits=None):
+    """Router gate: logits = x . w_gate^T (bf16 in, float32 out) on the tensor cores."""
+    _cuda(x, "x")
+    _cuda(w_gate, "w_gate")
+    if x.dtype != torch.bfloat16 or w_gate.dtype != torch.bfloat16:
+        raise TypeError("x and w_gate must be bfloat16")
+    T, H = x.shape
+    n = w_gate.shape[0]
+    if logits is None:
+        logits = torch.empty(T, n, dtype=torch.float32, device=x.device)
+    _check(lib().nvf_router_gemm(_ptr(x), _ptr(w_gate), T, H, n, _ptr(logits), logits.stride(0), _stream()))
+    return logits
+
+
+def moe_forward_gated(w: MoEWeights, x, w_gate, k: int, gs_a1, gs_a2, shared_gate=False, bias=None,
+                      renormalize=True, out_dtype=torch.float32, out=None, ws=None, cw=None):
+    """The layer from the hidden states: router gate, then the layer; shared_gate
+    scales the shared expert's output by sigmoid of the gate's last row."""
+    _cuda(x, "x")
+    _cuda(w_gate, "w_gate")
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, w.H, dtype=out_dtype, device=x.device)
+    if ws is None:
+        ws = workspace(T, w, k)
+    cw = w.c_struct() if cw is None else cw
+    _check(lib().nvfp4_moe_forward_gated(ctypes.byref(cw), _ptr(w_gate), int(shared_gate), _ptr(x), _ptr(bias), T, k,
+                                         int(renormalize), _ptr(gs_a1), _ptr(gs_a2),
+                                         NVF_F32 if out.dtype == torch.float32 else NVF_BF16, _ptr(out), _ptr(ws),
+                                         ws.numel(), _stream()))
     return out

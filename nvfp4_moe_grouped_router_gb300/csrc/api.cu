@@ -125,7 +125,7 @@ RouteArgs make_route_args(const float* logits, const float* bias, int32_t T, int
                           int32_t shared, int32_t* ids, float* w, int32_t* offsets, int32_t* tile_offsets,
                           int32_t* perm_to_src, int32_t* src_to_perm, int32_t* perm_token, void* scratch) {
   RouteArgs a{};
-  a.logits = logits; a.bias = bias; a.T = T; a.E = E; a.k = k; a.renormalize = renormalize ? 1 : 0;
+  a.logits = logits; a.ldl = E; a.bias = bias; a.T = T; a.E = E; a.k = k; a.renormalize = renormalize ? 1 : 0;
   a.shared = shared; a.ids = ids; a.weights = w; a.offsets = offsets; a.tile_offs = tile_offsets;
   a.perm_to_src = perm_to_src; a.src_to_perm = src_to_perm; a.perm_token = perm_token;
   const size_t W = (static_cast<size_t>(T) + 31) / 32;
@@ -417,14 +417,20 @@ nvf_status nvfp4_moe_workspace_layout(int32_t T, int32_t E, int32_t H, int32_t I
   L->a1 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), H));
   L->a2 = take(nvfp4_tiled_bytes(R, static_cast<int32_t>(Et), I));
   L->y = take(sizeof(float) * static_cast<size_t>(R) * H);
+  L->logits = take(sizeof(float) * static_cast<size_t>(T) * Et);
   L->total = off;
   return NVF_OK;
 }
 
-nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
-                             int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,
-                             int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
-                             void* const* stage_events, void* stream) {
+}  // extern "C"
+
+// The layer from routing to combine.  With w_gate the router gate runs first and
+// writes the logits into the workspace ([T, E + gated] rows); gated: the last
+// gate row's logit gates the shared expert.
+static nvf_status forward_impl(const nvf_moe_weights* w, const void* w_gate, int32_t gated, const void* x,
+                               const float* logits, const float* bias, int32_t T, int32_t k, int32_t renormalize,
+                               const float* gs_a1, const float* gs_a2, int32_t out_dtype, void* out, float* h_dump,
+                               void* ws, size_t ws_bytes, void* const* stage_events, void* stream) {
   NVF_BEGIN();
   NVF_REQUIRE(w != nullptr, "weights must not be NULL");
   nvf_moe_ws_layout L;
@@ -436,8 +442,11 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   NVF_REQUIRE(w->w13 && w->gs_w13 && w->w2 && w->gs_w2, "weight pointers must not be NULL");
   NVF_REQUIRE(aligned16(w->w13) && aligned16(w->w2), "weight buffers must be 16-byte aligned");
   NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
+  NVF_REQUIRE(gated == 0 || (gated == 1 && w->shared == 1), "shared_gate=%d needs a layer with a shared expert",
+              gated);
   if (T == 0) return NVF_OK;
-  NVF_REQUIRE(x && logits && gs_a1 && gs_a2 && out, "x, logits, gs_a1, gs_a2 and out must not be NULL");
+  NVF_REQUIRE(x && (logits || w_gate) && gs_a1 && gs_a2 && out, "x, logits (or w_gate), gs_a1, gs_a2 and out must not be NULL");
+  if (w_gate) NVF_REQUIRE(aligned16(w_gate), "w_gate must be 16-byte aligned");
   NVF_REQUIRE(aligned16(x) && aligned16(out) && (h_dump == nullptr || aligned16(h_dump)),
               "x, out and h_dump must be 16-byte aligned");
   NVF_REQUIRE(ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "ws must be 256-byte aligned");
@@ -460,6 +469,14 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
     return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, ev_flags)
                         : cudaSuccess;
   };
+  int64_t ldl = E;
+  if (w_gate) {
+    // router gate: logits (and the shared expert's gate logit) into the workspace
+    float* lg = reinterpret_cast<float*>(base + L.logits);
+    NVF_CUDA(launch_router_gemm(x, w_gate, T, H, E + gated, lg, E + gated, dev_->err, s), "router gate launch");
+    logits = lg;
+    ldl = E + gated;
+  }
   NVF_CUDA(mark(0), "cudaEventRecord");
 
   // routing, permutation and the activation quantization (A1) in one pass
@@ -467,6 +484,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
                                  reinterpret_cast<float*>(base + L.topk_w), i32(L.expert_offsets),
                                  i32(L.tile_offsets), i32(L.perm_to_src), i32(L.src_to_perm), i32(L.perm_token),
                                  base + L.route_scratch);
+  ra.ldl = ldl;
   ra.x = x;
   ra.H = H;
   ra.gs_a1 = gs_a1;
@@ -520,9 +538,44 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
   NVF_CUDA(mark(4), "cudaEventRecord");
 
   NVF_CUDA(launch_combine(base + L.y, H, reinterpret_cast<const float*>(base + L.topk_w),
-                          i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s, pdl),
+                          i32(L.src_to_perm), T, k, w->shared, out_dtype, out, s, pdl,
+                          gated ? logits + E : nullptr, ldl),
            "combine launch");
   NVF_CUDA(mark(5), "cudaEventRecord");
+  return NVF_OK;
+}
+
+extern "C" {
+
+nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const float* logits, const float* bias,
+                             int32_t T, int32_t k, int32_t renormalize, const float* gs_a1, const float* gs_a2,
+                             int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
+                             void* const* stage_events, void* stream) {
+  return forward_impl(w, nullptr, 0, x, logits, bias, T, k, renormalize, gs_a1, gs_a2, out_dtype, out, h_dump, ws,
+                      ws_bytes, stage_events, stream);
+}
+
+nvf_status nvfp4_moe_forward_gated(const nvf_moe_weights* w, const void* w_gate, int32_t shared_gate, const void* x,
+                                   const float* bias, int32_t T, int32_t k, int32_t renormalize, const float* gs_a1,
+                                   const float* gs_a2, int32_t out_dtype, void* out, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  g_msg[0] = 0;
+  NVF_REQUIRE(w_gate != nullptr, "w_gate must not be NULL");
+  return forward_impl(w, w_gate, shared_gate, x, nullptr, bias, T, k, renormalize, gs_a1, gs_a2, out_dtype, out,
+                      nullptr, ws, ws_bytes, nullptr, stream);
+}
+
+nvf_status nvf_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t H, int32_t n, float* logits,
+                           int64_t ldl, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(T >= 0 && n >= 1 && n <= 65535 * 32, "T=%d must be >= 0, n=%d in [1, 2097120]", T, n);
+  NVF_REQUIRE(H > 0 && H % 64 == 0, "H=%d must be a positive multiple of 64", H);
+  NVF_REQUIRE(ldl >= n, "ldl=%lld < n=%d", (long long)ldl, n);
+  if (T == 0) return NVF_OK;
+  NVF_REQUIRE(x && w_gate && logits, "x, w_gate and logits must not be NULL");
+  NVF_REQUIRE(aligned16(x) && aligned16(w_gate), "x and w_gate must be 16-byte aligned");
+  NVF_CUDA(launch_router_gemm(x, w_gate, T, H, n, logits, ldl, dev_->err, static_cast<cudaStream_t>(stream)),
+           "router gate launch");
   return NVF_OK;
 }
 

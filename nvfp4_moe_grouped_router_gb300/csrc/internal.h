@@ -53,7 +53,8 @@ cudaError_t launch_global_scale(const void* x, int x_dtype, int64_t groups, int6
                                 cudaStream_t s);
 
 struct RouteArgs {
-  const float* logits;      // [T, E]
+  const float* logits;      // [T, ldl]: row t's E logits first
+  int64_t ldl;              // logits row stride (elements), >= E
   const float* bias;        // nullable [E]
   int32_t T, E, k, renormalize, shared;
   int32_t* ids;             // [T, k]
@@ -78,9 +79,17 @@ size_t route_scratch_bytes(int32_t T, int32_t E);
 int route_kernel_launches(int32_t T, int32_t k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
-// y [R, H] and out [T, H] of the same dtype (X_F32 or X_BF16).
+// y [R, H] and out [T, H] of the same dtype (X_F32 or X_BF16).  shared_gate:
+// nullable; with a shared expert, its row is scaled by sigmoid(shared_gate[t * ldg])
+// instead of 1.
 cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const int32_t* src_to_perm, int32_t T,
-                           int32_t k, int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl);
+                           int32_t k, int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl,
+                           const float* shared_gate = nullptr, int64_t ldg = 0);
+
+// Router gate: logits[t * ldl + j] = sum_h x[t, h] * w_gate[j, h] (BF16 in, FP32 out),
+// j < n; H a multiple of 64.
+cudaError_t launch_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t H, int32_t n, float* logits,
+                               int64_t ldl, int* err, cudaStream_t s);
 
 enum GemmEpilogue : int { EPI_STORE_F32 = 0, EPI_STORE_BF16 = 1, EPI_SWIGLU_QUANT = 2 };
 

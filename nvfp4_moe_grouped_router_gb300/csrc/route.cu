@@ -418,7 +418,7 @@ __device__ __forceinline__ float y8_at(const Y8<BF16>& r, int e) {
 template <bool BF16>
 __global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* __restrict__ y, int H, const float* __restrict__ w,
                                                      const int32_t* __restrict__ s2p, int T, int k, int shared,
-                                                     void* out) {
+                                                     void* out, const float* __restrict__ sgate, int64_t ldg) {
   const int h8 = H >> 3;
   const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   const bool live = idx < static_cast<int64_t>(T) * h8;
@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* 
   int64_t row[kCombineSlots];
   float wv[kCombineSlots];
   int64_t srow = 0;
+  float sw = 1.0f;
   if (live) {
 #pragma unroll
     for (int j = 0; j < kCombineSlots; ++j)
@@ -436,7 +437,11 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* 
         wv[j] = __ldg(w + a);
         row[j] = static_cast<int64_t>(__ldg(s2p + a)) * H + c * 8;
       }
-    if (shared) srow = static_cast<int64_t>(__ldg(s2p + static_cast<int64_t>(T) * k + t)) * H + c * 8;
+    if (shared) {
+      srow = static_cast<int64_t>(__ldg(s2p + static_cast<int64_t>(T) * k + t)) * H + c * 8;
+      // gated shared expert: sigmoid of the token's gate logit (written by the router, before this launch)
+      if (sgate != nullptr) sw = 1.0f / (1.0f + expf(-__ldg(sgate + static_cast<int64_t>(t) * ldg)));
+    }
   }
   griddep_wait();
   if (!live) return;
@@ -462,8 +467,13 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* 
   }
   if (shared) {
     const Y8<BF16> v = load_y8_raw<BF16>(y, srow);
+    if (sgate == nullptr) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += y8_at<BF16>(v, e);
+      for (int e = 0; e < 8; ++e) acc[e] += y8_at<BF16>(v, e);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(sw, y8_at<BF16>(v, e), acc[e]);
+    }
   }
   if constexpr (BF16) {
     uint32_t u[4];
@@ -549,14 +559,15 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const int32_t* s2p, int32_t T, int32_t k,
-                           int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl) {
+                           int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl, const float* shared_gate,
+                           int64_t ldg) {
   if (T == 0) return cudaSuccess;
   const int64_t total = static_cast<int64_t>(T) * (H / 8);
   const int64_t blocks = (total + 255) / 256;   // one output group per thread (T <= 2^24, H <= 2^20: fits the grid)
   auto kern = dtype == X_BF16 ? combine_kernel<true> : combine_kernel<false>;
   prefer_max_shared(reinterpret_cast<const void*>(kern));
   return launch_kernel(kern, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, pdl, y, H, weights, s2p, T, k,
-                       shared, out);
+                       shared, out, shared_gate, ldg);
 }
 
 }  // namespace nvf

@@ -25,14 +25,15 @@ __device__ __forceinline__ uint32_t logit_key(float f) {
 // What the top-k reads and writes, small enough to stay in registers (a copy
 // of the whole argument block would live in local memory).
 struct TopkIO {
-  const float* logits;   // [T, E]
+  const float* logits;   // [T, ldl]
+  int64_t ldl;
   const float* bias;     // nullable [E]
   int32_t E, k, renormalize;
   int32_t* ids;          // nullable [T, k]: ids and weights are written when set
   float* weights;        // [T, k]
 };
 __device__ __forceinline__ TopkIO topk_io(const RouteArgs& a, bool write) {
-  return TopkIO{a.logits, a.bias, a.E, a.k, a.renormalize, write ? a.ids : nullptr, a.weights};
+  return TopkIO{a.logits, a.ldl, a.bias, a.E, a.k, a.renormalize, write ? a.ids : nullptr, a.weights};
 }
 
 // Top-k of NT tokens by one warp (the routing kernels use NT = 1).  Each round takes the warp maximum of the remaining keys with one
@@ -52,7 +53,7 @@ __device__ __forceinline__ void topk_tokens(const TopkIO a, const int (&tt)[NT],
 #pragma unroll
   for (int q = 0; q < NT; ++q) {
     taken[q] = 0u;
-    const float* row = a.logits + static_cast<int64_t>(tt[q] < 0 ? 0 : tt[q]) * E;
+    const float* row = a.logits + static_cast<int64_t>(tt[q] < 0 ? 0 : tt[q]) * a.ldl;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = i * 32 + lane;

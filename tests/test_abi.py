@@ -58,9 +58,10 @@ def test_workspace_layout(nvf):
     L = nvf.workspace_layout(256, 512, 4096, 1024, 10, True)
     assert L["R"] == 256 * 11
     offs = [L[n] for n in ("topk_ids", "topk_w", "expert_offsets", "tile_offsets", "perm_to_src", "src_to_perm",
-                           "perm_token", "route_scratch", "tile_group", "a1", "a2", "y")]
+                           "perm_token", "route_scratch", "tile_group", "a1", "a2", "y", "logits")]
     assert all(o % 256 == 0 for o in offs)
-    assert offs == sorted(offs) and L["total"] > offs[-1] + L["R"] * 4096 * 4 - 256
+    assert offs == sorted(offs) and L["logits"] >= L["y"] + L["R"] * 4096 * 4
+    assert L["total"] >= L["logits"] + 256 * 513 * 4
     with pytest.raises(nvf.NvfError):
         nvf.workspace_layout(16, 8, 200, 128, 2, False)       # H not a multiple of 128
     with pytest.raises(nvf.NvfError):
