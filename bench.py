@@ -347,6 +347,55 @@ def dense_sweep(args):
               flush=True)
 
 
+def router_sweep(args):
+    """The router gate (the step before routing) on the bench layer's shape:
+    x bf16 [T, 2048] . w_gate bf16 [129, 2048]^T (128 routed experts + one
+    shared-expert gate row) for the decode and prefill batches.  One JSON line
+    per T with the time per call (CUDA graph of the calls), the bf16 FLOP rate
+    and the bytes moved (x, w_gate, logits) against the measured peaks."""
+    import nvfp4_moe_grouped_router_gb300 as nvf
+    from nvfp4_moe_grouped_router_gb300 import build as nvf_build
+    torch.cuda.set_device(0)
+    nvf_build.build()
+    nvf.lib()
+    hbm, bf16, src = load_peaks()
+    H, n = 2048, 129
+    g = torch.Generator().manual_seed(0)
+    w = (torch.randn(n, H, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    stream = torch.cuda.Stream()
+    for T in (32, 4096):
+        x = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+        lg = torch.empty(T, n, device="cuda")
+        steps = max(3, min(args.steps, 500))
+        for _ in range(max(3, args.warmup)):
+            nvf.router_gemm(x, w, logits=lg)
+        torch.cuda.synchronize()
+        stream.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(steps):
+                nvf.router_gemm(x, w, logits=lg)
+        torch.cuda.current_stream().wait_stream(stream)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        code, detail = nvf.device_status()
+        if code != 0:
+            raise RuntimeError(f"device error word {code} at {detail}")
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        nbytes = T * H * 2 + n * H * 2 + T * n * 4
+        print(json.dumps({"metric": "router gate x . w_gate^T (bf16, H=2048, 128 + 1 rows): us per call", "T": T,
+                          "us_per_call": us, "tflops": 2.0 * T * H * n / (us * 1e-6) / 1e12,
+                          "tc_frac_bf16": 2.0 * T * H * n / (us * 1e-6) / 1e12 / bf16,
+                          "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm,
+                          "peak_source": src, "steps": steps, "launches_per_call": 1, "data": "synthetic"}),
+              flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,9 +408,12 @@ def main():
                     help="plain launches of W + K steps and nothing else (for ncu launch lists / captures)")
     ap.add_argument("--dense", action="store_true",
                     help="the dense W4A4 linear sweep (N=34816, K=5120, M=1..4096) instead of the MoE layer")
+    ap.add_argument("--router", action="store_true", help="the router gate GEMM at the decode and prefill batches")
     args = ap.parse_args()
     if args.dense:
         return dense_sweep(args)
+    if args.router:
+        return router_sweep(args)
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
