@@ -310,7 +310,7 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
  * w_gate[j, h] for j < n, with BF16 inputs multiplied on the tensor cores and
  * summed in FP32.
  *   x       device bf16 [T, H] (row pitch H), 16-byte aligned; H a positive
- *           multiple of 64.
+ *           multiple of 128.
  *   w_gate  device bf16 [n, H]: one row per routed expert, plus, for a gated
  *           shared expert, one more row whose logit gates it.
  *   logits  device float [T, ldl], ldl >= n; columns j < n are written.

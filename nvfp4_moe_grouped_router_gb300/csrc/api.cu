@@ -569,7 +569,7 @@ nvf_status nvf_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t
                            int64_t ldl, void* stream) {
   NVF_BEGIN();
   NVF_REQUIRE(T >= 0 && n >= 1 && n <= 65535 * 32, "T=%d must be >= 0, n=%d in [1, 2097120]", T, n);
-  NVF_REQUIRE(H > 0 && H % 64 == 0, "H=%d must be a positive multiple of 64", H);
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
   NVF_REQUIRE(ldl >= n, "ldl=%lld < n=%d", (long long)ldl, n);
   if (T == 0) return NVF_OK;
   NVF_REQUIRE(x && w_gate && logits, "x, w_gate and logits must not be NULL");

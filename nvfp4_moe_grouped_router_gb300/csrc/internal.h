@@ -87,7 +87,7 @@ cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const
                            const float* shared_gate = nullptr, int64_t ldg = 0);
 
 // Router gate: logits[t * ldl + j] = sum_h x[t, h] * w_gate[j, h] (BF16 in, FP32 out),
-// j < n; H a multiple of 64.
+// j < n; H a multiple of 128.
 cudaError_t launch_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t H, int32_t n, float* logits,
                                int64_t ldl, int* err, cudaStream_t s);
 
