@@ -155,6 +155,28 @@ def grouped_gemm(a_codes, a_scales, offsets, gs_a, w_codes, w_scales, gs_w):
     return out
 
 
+def w4a16_matmul(a, w_codes, w_scales, gs_w):
+    """Weight-only NVFP4 product (the W4A16 decode alternative the pages compare
+    against, e.g. Marlin W4A16 in FlashInfer issue #2723, "Speed Comparison",
+    and the W4A16 columns of the unsloth report's per-GEMM table):
+    D = gs_w * (A . dW^T) with A the bf16 activations (as exact float values,
+    no quantization) and dW = e2m1 * e4m3 of the weight blocks.  Every product
+    is exact in float64 and the sum is float64."""
+    a = np.asarray(a, dtype=np.float64)
+    return np.float64(F32(gs_w)) * (a @ F.dequantize_rows(w_codes, w_scales).T)
+
+
+def grouped_w4a16(a, offsets, w_codes, w_scales, gs_w):
+    """D[p] = w4a16_matmul(A[p], W_e) for the rows p of group e (float64)."""
+    G, N = w_codes.shape[0], w_codes.shape[1]
+    out = np.zeros((np.asarray(a).shape[0], N), dtype=np.float64)
+    for e in range(G):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            out[lo:hi] = w4a16_matmul(np.asarray(a)[lo:hi], w_codes[e], w_scales[e], gs_w[e])
+    return out
+
+
 def swiglu(c1, I: int) -> np.ndarray:
     """h = silu(g) * u = g / (1 + exp(-g)) * u, float64, for g = C1[:, :I], u = C1[:, I:]."""
     c1 = np.asarray(c1, dtype=np.float64)
