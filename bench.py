@@ -396,6 +396,84 @@ def router_sweep(args):
               flush=True)
 
 
+def _graph_time_us(fn, steps, warmup):
+    """Mean microseconds per call of fn, replayed as one CUDA graph of `steps` calls."""
+    for _ in range(max(3, warmup)):
+        fn(0)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            fn(i)
+    torch.cuda.current_stream().wait_stream(stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps
+
+
+def w4a16_sweep(args):
+    """The weight-only path (FP16 activations x NVFP4 weights dequantized in the
+    kernel) beside the W4A4 GEMM on the same weight bytes: (1) the decode layer's
+    gate_up GEMM (its routing's expert groups, x gathered in permuted order and
+    rounded to FP16); (2) the pages' dense gate_up shape N = 34816, K = 5120,
+    three weight copies rotating so that weights stream from HBM.  One JSON line
+    per case."""
+    import nvfp4_moe_grouped_router_gb300 as nvf
+    from nvfp4_moe_grouped_router_gb300 import build as nvf_build
+    torch.cuda.set_device(0)
+    nvf_build.build()
+    nvf.lib()
+    hbm, bf16, src = load_peaks()
+    steps = max(3, min(args.steps, 200))
+    cfg = CONFIGS["decode"]
+    w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, cfg.shared, lambda e: expert_weights(cfg, e, 0, device="cuda"))
+    x, logits, _ = make_inputs(cfg, 0, device="cpu")
+    x, logits = x.cuda(), logits.cuda()
+    r = nvf.route_permute(logits, cfg.k)
+    offs, tiles = r["expert_offsets"], r["tile_offsets"]
+    touched = int((offs[1:] > offs[:-1]).sum().item())
+    A = x[r["perm_token"].long()].to(torch.float16).contiguous()
+    D = torch.empty(cfg.R, 2 * cfg.I, device="cuda")
+    us = _graph_time_us(lambda i: nvf.w4a16_grouped_gemm(A, w.w13, w.gs_w13, offs, tiles, 2 * cfg.I, cfg.H, D=D),
+                        steps, args.warmup)
+    nbytes = gemm1_bytes(cfg, touched)
+    print(json.dumps({"metric": "W4A16 grouped GEMM, decode layer gate_up (N=1536, K=2048, 256 rows in "
+                                f"{touched} experts): us per call", "us_per_call": us,
+                      "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm,
+                      "algorithmic_bytes": nbytes, "peak_source": src, "steps": steps}), flush=True)
+    del w
+    N, K = DENSE_N, DENSE_K
+    g = torch.Generator(device="cuda").manual_seed(0)
+    copies = []
+    for _ in range(3):
+        wd = torch.randn(N, K, generator=g, device="cuda") * 0.02
+        gs_w = torch.tensor([wd.abs().max().item() / 2688.0], dtype=torch.float32, device="cuda")
+        B, _ = nvf.quantize(wd, gs_w, layout=nvf.LAYOUT_TILED)
+        copies.append((B, gs_w))
+        del wd
+    w_bytes = nvf.tiled_bytes(N, 0, K)
+    for Mr in DENSE_M:
+        a = torch.randn(Mr, K, generator=g, device="cuda").to(torch.bfloat16).to(torch.float16)
+        o = torch.tensor([0, Mr], dtype=torch.int32, device="cuda")
+        t = torch.tensor([0, (Mr + 127) // 128], dtype=torch.int32, device="cuda")
+        Dd = torch.empty(Mr, N, device="cuda")
+        n = steps if Mr < 1024 else min(steps, 40)
+        us = _graph_time_us(lambda i: nvf.w4a16_grouped_gemm(a, copies[i % 3][0], copies[i % 3][1], o, t, N, K, D=Dd),
+                            n, args.warmup)
+        tflops = 2.0 * Mr * N * K / (us * 1e-6) / 1e12
+        gbs = (w_bytes + Mr * K * 2 + Mr * N * 4) / (us * 1e-6) / 1e9
+        print(json.dumps({"metric": "W4A16 dense linear (gate_up N=34816 K=5120): us per call", "M": Mr,
+                          "us_per_call": us, "tflops": tflops, "tc_frac_bf16": tflops / bf16, "gbs": gbs,
+                          "hbm_frac": gbs / hbm, "peak_source": src, "steps": n}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,7 +487,10 @@ def main():
     ap.add_argument("--dense", action="store_true",
                     help="the dense W4A4 linear sweep (N=34816, K=5120, M=1..4096) instead of the MoE layer")
     ap.add_argument("--router", action="store_true", help="the router gate GEMM at the decode and prefill batches")
+    ap.add_argument("--w4a16", action="store_true", help="the weight-only (W4A16) GEMM beside W4A4")
     args = ap.parse_args()
+    if args.w4a16:
+        return w4a16_sweep(args)
     if args.dense:
         return dense_sweep(args)
     if args.router:

@@ -255,6 +255,22 @@ nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B
                               const float* gs_b, const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G,
                               int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream);
 
+/* Weight-only NVFP4 grouped GEMM (W4A16), the decode alternative the pages
+ * compare with the W4A4 path: FP16 activations times NVFP4 weights
+ * dequantized in the kernel to FP16 (every e2m1 * e4m3 product is exact in
+ * FP16) on the tensor cores (unsloth report, SASS paragraph under "Why it
+ * matters": W4A16 unpacks FP4 and runs FP16 MMA; Marlin W4A16 in FlashInfer
+ * issue #2723, "Speed Comparison"):
+ *   D[row, n] = gs_b[g] * sum_k A[row, k] * dB_g[n, k]   for offsets[g] <= row < offsets[g+1].
+ *   A       device fp16 [a_rows, lda], 16-byte aligned, lda >= K and a multiple
+ *           of 8 (BF16 activations are converted to FP16, round to nearest, by
+ *           the caller).
+ *   B, gs_b, group_offsets, tile_offsets, G, N, K, out_dtype, D, ldd as
+ *           nvfp4_grouped_gemm (B the TILED weights of G groups of N rows). */
+nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
+                                    const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G, int32_t N,
+                                    int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream);
+
 /* Prepared expert weights (all device pointers). */
 typedef struct nvf_moe_weights {
   int32_t E;               /* routed experts */

@@ -45,6 +45,8 @@ SIGNATURES = {
     "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
                                          _P]),
     "nvf_router_gemm": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P]),
+    "nvfp4_w4a16_grouped_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
+                                                _P]),
     "nvfp4_moe_forward_gated": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ,
                                                _P]),
 }
@@ -206,6 +208,22 @@ def grouped_gemm(A, a_rows: int, B, gs_a, gs_b, offsets, tile_offsets, N: int, K
     code = NVF_F32 if D.dtype == torch.float32 else NVF_BF16
     _check(lib().nvfp4_grouped_gemm(_ptr(A), a_rows, _ptr(B), _ptr(gs_a), _ptr(gs_b), _ptr(offsets),
                                     _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0), _stream()))
+    return D
+
+
+def w4a16_grouped_gemm(A, B, gs_b, offsets, tile_offsets, N: int, K: int, out_dtype=torch.float32, D=None):
+    """D[row] = gs_b[g] A[row] . dB[g]^T for the rows of group g: A fp16 [rows, K]
+    (row-major, grouped by offsets), B the TILED weights of the groups."""
+    _cuda(A, "A")
+    if A.dtype != torch.float16:
+        raise TypeError("A must be float16")
+    G = offsets.numel() - 1
+    rows = A.shape[0]
+    if D is None:
+        D = torch.zeros(max(rows, 1), N, dtype=out_dtype, device=A.device)
+    code = NVF_F32 if D.dtype == torch.float32 else NVF_BF16
+    _check(lib().nvfp4_w4a16_grouped_gemm(_ptr(A), rows, A.stride(0), _ptr(B), _ptr(gs_b), _ptr(offsets),
+                                          _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0), _stream()))
     return D
 
 

@@ -41,34 +41,6 @@ constexpr int A_STAGE = RATOMS * A_ATOM;  // 16 KB
 constexpr int B_STAGE = RATOMS * B_ATOM;  // 4 KB
 constexpr int R_SMEM = RSTAGES * (A_STAGE + B_STAGE) + 1024 + 64;
 
-// Instruction descriptor of a kind::f16 MMA: D FP32 (bits 4-5 = 1), A and B
-// BF16 (bits 7-9 and 10-12 = 1), both K-major, N >> 3 in bits 17-22, M >> 4 in
-// bits 24-28.
-__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-// Shared-memory writes made by these threads become visible to the tensor core (async proxy).
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(addr), "r"(0) : "memory");
-}
-
 __global__ void __launch_bounds__(R_THREADS) router_gemm_kernel(const __nv_bfloat16* __restrict__ x,
                                                                 const __nv_bfloat16* __restrict__ wg, int T, int H,
                                                                 int n, float* __restrict__ logits, int64_t ldl,
@@ -117,7 +89,7 @@ __global__ void __launch_bounds__(R_THREADS) router_gemm_kernel(const __nv_bfloa
     }
   };
 
-  const uint32_t idesc = bf16_idesc(RM, RN);
+  const uint32_t idesc = f16kind_idesc(RM, RN, true);
   bool ok = true;
   for (int kb = 0; kb < RSTAGES - 1; ++kb) {
     if (kb < nkb) load_stage(kb);
@@ -133,7 +105,7 @@ __global__ void __launch_bounds__(R_THREADS) router_gemm_kernel(const __nv_bfloa
 #pragma unroll
       for (int kk = 0; kk < RK / 16; ++kk) {
         const int at = kk >> 2, ks = kk & 3;     // swizzle atom, 16-element step inside it
-        tc_mma_bf16(tmem, operand_desc_sw128(a0 + s * A_STAGE + at * A_ATOM + ks * 32),
+        tc_mma_f16kind(tmem, operand_desc_sw128(a0 + s * A_STAGE + at * A_ATOM + ks * 32),
                     operand_desc_sw128(b0 + s * B_STAGE + at * B_ATOM + ks * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
       }
       tc_commit(bar0 + 8 * s);
