@@ -175,18 +175,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& p, const Sche
   return x;
 }
 
-// Bounded wait that ignores the abort flag (used when draining).
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err, int detail) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-      report_error(err, DEV_TIMEOUT_DRAIN, detail);
-      return false;
-    }
-  }
-  return true;
-}
 
 // The scales of one K tile (four 64-element K steps), as the MMA reads them
 // from TMEM.  Scale atom (512 bytes, one per K step and 128 rows): 16 bytes per
@@ -206,7 +194,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Load atoms `src + kk * 512` (kk < 4), row `lane`, into v[4 kk .. 4 kk + 3].
 __device__ __forceinline__ void load_atom_rows(uint32_t (&v)[16], const uint8_t* src, int lane) {

@@ -99,6 +99,21 @@ def test_decode_shape(nvf):
     assert rel_err(D, M.grouped_w4a16(a.astype(np.float64), offs, w_c, w_s, gs_w)) <= TOL
 
 
+@pytest.mark.parametrize("N,K", [(640, 320), (1536, 512)])
+def test_many_items_per_cta(nvf, N, K):
+    """More work items (token tile x weight pair) than SMs: every CTA runs
+    several, so the rings wrap across items; N = 640 ends each group with an
+    unpaired weight tile, K = 320 with a partial K tile; one group spans three
+    token tiles."""
+    rng = np.random.default_rng(N + K)
+    sizes = list(rng.integers(0, 4, 150)) + [300] + list(rng.integers(0, 3, 50))
+    G, R = len(sizes), int(sum(sizes))
+    a = torch.randn(R, K, generator=torch.Generator().manual_seed(N)).to(torch.float16).numpy()
+    w_c, w_s, gs_w = _random_weights(rng, G, N, K)
+    D, offs = _run(nvf, a, sizes, w_c, w_s, gs_w)
+    assert rel_err(D, M.grouped_w4a16(a.astype(np.float64), offs, w_c, w_s, gs_w)) <= TOL
+
+
 def test_argument_validation(nvf):
     z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     a = torch.zeros(4, 100, dtype=torch.float16, device="cuda")
