@@ -22,4 +22,4 @@ itself: closed forms of the formats, torch's float8 cast, independent scalar
 encoders, brute-force sorts and exact rational arithmetic.  Every function here
 is pinned; none is "parity unpinned".
 """
-from . import formats, moe  # noqa: F401
+from . import ep, formats, moe  # noqa: F401
