@@ -348,6 +348,97 @@ nvf_status nvfp4_moe_forward_gated(const nvf_moe_weights* w, const void* w_gate,
                                    const float* gs_a2, int32_t out_dtype, void* out, void* ws, size_t ws_bytes,
                                    void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Expert parallelism (EP): the data movement around the token all-to-all the
+ * pages run with DeepEP (vLLM PR #35737, CI failure logs: all2all_manager
+ * get_handle, the deepep_high_throughput MoE prepare/finalize).  The pages show
+ * the call sites, not the layout; the reading implemented here:
+ *   G ranks, each routing its own T tokens over all E routed experts (E a
+ *   multiple of G); rank r owns routed experts [r E/G, (r+1) E/G); a shared
+ *   expert is replicated and every rank computes its own tokens' shared rows.
+ *   A rank sends each (token, slot) row, NVFP4-quantized with the destination
+ *   expert's activation global scale, to the expert's owner; the receiver
+ *   groups what arrives by local expert (source by source) and runs its local
+ *   experts; each y row returns to its sender at the position it was sent
+ *   from, and the sender combines as on one GPU.
+ * One EP layer on rank r:
+ *   moe_route_permute (global expert ids) -> nvf_ep_dispatch ->
+ *   exchange send_counts, then the rows (the caller's all-to-all) ->
+ *   nvf_ep_receive -> nvfp4_moe_experts (local weights) -> nvf_ep_return ->
+ *   exchange back -> nvf_moe_combine (with src_to_send).
+ * Every call is asynchronous on `stream` and allocates nothing.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of one exchanged A1 row: H/2 code bytes (element 2j in the low nibble
+ * of byte j), then H/16 E4M3 scale bytes, padded to a multiple of 16. */
+size_t nvf_ep_row_bytes(int32_t H);
+
+/* Dispatch on rank `rank` of G.  Inputs are moe_route_permute's outputs for
+ * the rank's T tokens (expert_offsets [E + shared + 1], perm_token and
+ * perm_to_src [R], R = T*k + shared*T), x (device bf16 [T, H], 16-byte aligned,
+ * H a positive multiple of 128) and gs_a1 (device float [E + shared], global
+ * expert ids).  Outputs (device, caller-owned):
+ *   send_rows   [R, nvf_ep_row_bytes(H)] bytes, 16-byte aligned: the rows for
+ *               rank 0, then rank 1, ...; rank r's rows are its experts' rows
+ *               in routing order; the rank's own segment ends with its shared
+ *               rows (by token);
+ *   send_counts int32 [G, E/G + 1]: rows for each local expert of each
+ *               destination; column E/G is the shared expert (own rank only);
+ *   src_to_send int32 [R]: send position of assignment a (a = t*k + j, shared
+ *               rows T*k + t), the row index the combine reads.
+ * Errors: NVF_ERR_INVALID_ARG (G < 1, G > 1024, E % G != 0, rank out of
+ * range, NULL or misaligned buffers), NVF_ERR_UNSUPPORTED_DEVICE, NVF_ERR_CUDA. */
+nvf_status nvf_ep_dispatch(const void* x, int32_t T, int32_t H, int32_t E, int32_t k, int32_t shared, int32_t G,
+                           int32_t rank, const int32_t* expert_offsets, const int32_t* perm_token,
+                           const int32_t* perm_to_src, const float* gs_a1, void* send_rows, int32_t* send_counts,
+                           int32_t* src_to_send, void* stream);
+
+/* int32 words of scratch nvf_ep_receive needs: 2 * G * (El + 1). */
+size_t nvf_ep_receive_scratch_words(int32_t G, int32_t El);
+
+/* Receive on a rank with El local routed experts (+ the shared one when
+ * shared = 1).  recv_rows: device [n_recv, nvf_ep_row_bytes(H)], the rows from
+ * source 0, then source 1, ... (each source's send segment for this rank);
+ * recv_counts: device int32 [G, El + 1], row s = source s's send_counts row for
+ * this rank; n_recv = the sum of recv_counts (a larger n_recv is reported
+ * through nvf_device_status, code 5, and the extra rows are ignored).
+ * Outputs (device, caller-owned): a1, the local experts' A operand in
+ * NVF_LAYOUT_TILED_GROUPED (nvfp4_tiled_bytes(n_recv, El + shared, H) bytes,
+ * 16-byte aligned); local_offsets and local_tile_offsets int32
+ * [El + shared + 1] (local expert j's rows: source 0's, then source 1's, ...);
+ * recv_to_grp int32 [n_recv], received row i's grouped row.  scratch: device
+ * int32 [nvf_ep_receive_scratch_words(G, El)]. */
+nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* recv_counts, int32_t G, int32_t El,
+                          int32_t shared, int32_t H, uint8_t* a1, int32_t* local_offsets,
+                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, void* stream);
+
+/* The expert computation of steps 4-6 on grouped rows (the layer's GEMMs
+ * without routing): y[p] = alpha2_e * A2_p . W2_e^T with A2 the NVFP4 of
+ * silu(gate) * up of alpha1_e * A1_p . W13_e^T, for the rows p of local
+ * expert e.  w: the (local) experts' prepared weights; a1: device
+ * NVF_LAYOUT_TILED_GROUPED [a_rows, H] rows grouped by offsets / tile_offsets
+ * (int32 [E + shared + 1], device); gs_a1, gs_a2: device float [E + shared];
+ * y: device [a_rows, H] of out_dtype (NVF_F32 | NVF_BF16), 16-byte aligned;
+ * ws: device scratch of nvfp4_tiled_bytes(a_rows, E + shared, I) bytes
+ * (the A2 operand), 256-byte aligned. */
+nvf_status nvfp4_moe_experts(const nvf_moe_weights* w, const uint8_t* a1, int64_t a_rows, const int32_t* offsets,
+                             const int32_t* tile_offsets, const float* gs_a1, const float* gs_a2, int32_t out_dtype,
+                             void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Return: y_ret[i] = y[recv_to_grp[i]] (rows of H elements of dtype NVF_F32 or
+ * NVF_BF16, device, 16-byte aligned), the received order, which the return
+ * exchange sends back segment by segment. */
+nvf_status nvf_ep_return(const void* y, int64_t n_recv, int32_t H, int32_t dtype, const int32_t* recv_to_grp,
+                         void* y_ret, void* stream);
+
+/* Step 7 on its own: out[t] = sum_j w[t, j] y[src_to_row[t*k + j]] (+ the
+ * shared row y[src_to_row[T*k + t]]), FP32 sums in slot order.  y: device
+ * [rows, H] of dtype (NVF_F32 | NVF_BF16), 32-byte aligned rows (H a multiple
+ * of 128); topk_w: device float [T, k]; src_to_row: device int32
+ * [T*k + shared*T]; out: device [T, H] of dtype. */
+nvf_status nvf_moe_combine(const void* y, int32_t H, int32_t dtype, const float* topk_w, const int32_t* src_to_row,
+                           int32_t T, int32_t k, int32_t shared, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

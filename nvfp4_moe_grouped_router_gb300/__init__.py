@@ -49,6 +49,14 @@ SIGNATURES = {
                                                 _P]),
     "nvfp4_moe_forward_gated": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ,
                                                _P]),
+    "nvf_ep_row_bytes": (_SZ, [_I32]),
+    "nvf_ep_receive_scratch_words": (_SZ, [_I32, _I32]),
+    "nvf_ep_dispatch": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                       _P]),
+    "nvf_ep_receive": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "nvfp4_moe_experts": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "nvf_ep_return": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
+    "nvf_moe_combine": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _P]),
 }
 
 
@@ -335,3 +343,125 @@ def moe_forward_gated(w: MoEWeights, x, w_gate, k: int, gs_a1, gs_a2, shared_gat
                                          NVF_F32 if out.dtype == torch.float32 else NVF_BF16, _ptr(out), _ptr(ws),
                                          ws.numel(), _stream()))
     return out
+
+
+# ----------------------------------------------------------------------------- expert parallelism
+# Rank r of G owns routed experts [r E/G, (r+1) E/G); a shared expert is
+# replicated.  The device steps are the library's; the exchanges below are
+# torch.distributed all-to-alls (NCCL between GPUs, gloo between CPU ranks).
+
+def ep_row_bytes(H: int) -> int:
+    return int(lib().nvf_ep_row_bytes(H))
+
+
+def ep_dispatch(x, route: dict, E: int, k: int, shared: bool, G: int, rank: int, gs_a1):
+    """Quantized send rows (ranks' segments back to back), send_counts [G, E/G+1]
+    and src_to_send [R] from one rank's tokens and routing."""
+    _cuda(x, "x")
+    T, H = x.shape
+    R = T * k + (T if shared else 0)
+    dev = x.device
+    send = torch.empty(max(R, 1), ep_row_bytes(H), dtype=torch.uint8, device=dev)
+    counts = torch.empty(G, E // G + 1, dtype=torch.int32, device=dev)
+    s2s = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
+    _check(lib().nvf_ep_dispatch(_ptr(x), T, H, E, k, int(shared), G, rank, _ptr(route["expert_offsets"]),
+                                 _ptr(route["perm_token"]), _ptr(route["perm_to_src"]), _ptr(gs_a1), _ptr(send),
+                                 _ptr(counts), _ptr(s2s), _stream()))
+    return send[:R], counts, s2s[:R]
+
+
+def ep_receive(recv_rows, recv_counts, El: int, shared: bool, H: int, n_recv: int):
+    """Group the arriving rows by local expert: A1 (TILED_GROUPED), local offsets,
+    local tile offsets and recv_to_grp."""
+    G = recv_counts.shape[0]
+    dev = recv_counts.device
+    Et = El + int(shared)
+    a1 = torch.empty(max(tiled_bytes(n_recv, Et, H), 16), dtype=torch.uint8, device=dev)
+    off = torch.empty(Et + 1, dtype=torch.int32, device=dev)
+    toff = torch.empty(Et + 1, dtype=torch.int32, device=dev)
+    r2g = torch.empty(max(n_recv, 1), dtype=torch.int32, device=dev)
+    scratch = torch.empty(int(lib().nvf_ep_receive_scratch_words(G, El)), dtype=torch.int32, device=dev)
+    _check(lib().nvf_ep_receive(_ptr(recv_rows), n_recv, _ptr(recv_counts), G, El, int(shared), H, _ptr(a1), _ptr(off),
+                                _ptr(toff), _ptr(r2g), _ptr(scratch), _stream()))
+    return dict(a1=a1, offsets=off, tile_offsets=toff, recv_to_grp=r2g[:n_recv], n=n_recv)
+
+
+def moe_experts(w: MoEWeights, a1, a_rows: int, offsets, tile_offsets, gs_a1, gs_a2, out_dtype=torch.float32):
+    """Steps 4-6 on grouped rows: y [a_rows, H]."""
+    dev = a1.device
+    y = torch.empty(max(a_rows, 1), w.H, dtype=out_dtype, device=dev)
+    ws = torch.empty(max(tiled_bytes(a_rows, w.E + int(w.shared), w.I), 256), dtype=torch.uint8, device=dev)
+    cw = w.c_struct()
+    _check(lib().nvfp4_moe_experts(ctypes.byref(cw), _ptr(a1), a_rows, _ptr(offsets), _ptr(tile_offsets), _ptr(gs_a1),
+                                   _ptr(gs_a2), NVF_F32 if out_dtype == torch.float32 else NVF_BF16, _ptr(y), _ptr(ws),
+                                   ws.numel(), _stream()))
+    return y[:a_rows]
+
+
+def ep_return(y, recv_to_grp):
+    """y rows back in received order."""
+    n, H = y.shape
+    out = torch.empty(max(n, 1), H, dtype=y.dtype, device=y.device)
+    _check(lib().nvf_ep_return(_ptr(y), n, H, NVF_F32 if y.dtype == torch.float32 else NVF_BF16, _ptr(recv_to_grp),
+                               _ptr(out), _stream()))
+    return out[:n]
+
+
+def moe_combine(y, topk_w, src_to_row, T: int, k: int, shared: bool):
+    """out[t] = sum_j w[t,j] y[src_to_row[t*k+j]] (+ the shared row), FP32 sums."""
+    H = y.shape[1]
+    out = torch.empty(T, H, dtype=y.dtype, device=y.device)
+    _check(lib().nvf_moe_combine(_ptr(y), H, NVF_F32 if y.dtype == torch.float32 else NVF_BF16, _ptr(topk_w),
+                                 _ptr(src_to_row), T, k, int(shared), _ptr(out), _stream()))
+    return out
+
+
+def ep_exchange_counts(send_counts, group=None):
+    """All-to-all of the per-destination count rows: recv_counts[s] = source s's
+    send_counts row for this rank."""
+    import torch.distributed as dist
+    recv = torch.empty_like(send_counts)
+    dist.all_to_all_single(recv, send_counts.contiguous(), group=group)
+    return recv
+
+
+def ep_exchange_rows(send, send_splits, recv_splits, group=None):
+    """All-to-all of row buffers: send's first send_splits[0] rows go to rank 0,
+    ...; returns the rows from every source back to back."""
+    import torch.distributed as dist
+    recv = torch.empty((sum(recv_splits),) + tuple(send.shape[1:]), dtype=send.dtype, device=send.device)
+    dist.all_to_all_single(recv, send.contiguous(), list(recv_splits), list(send_splits), group=group)
+    return recv
+
+
+def ep_local_scales(gs, E: int, G: int, rank: int, shared: bool):
+    """The local experts' entries of a per-expert vector [E + shared]."""
+    El = E // G
+    parts = [gs[rank * El:(rank + 1) * El]] + ([gs[E:E + 1]] if shared else [])
+    return torch.cat(parts).contiguous()
+
+
+def ep_forward(w_local: MoEWeights, x, logits, k: int, E: int, gs_a1, gs_a2, shared=False, renormalize=True,
+               out_dtype=torch.float32, group=None):
+    """The layer with expert parallelism on this rank: route over all E experts,
+    dispatch, exchange, the local experts, return, exchange back, combine.
+    w_local: this rank's E/G experts (and the shared one); gs_a1, gs_a2: the
+    layer's per-expert scales [E + shared] (global ids)."""
+    import torch.distributed as dist
+    G, rank = dist.get_world_size(group), dist.get_rank(group)
+    T, H = x.shape
+    El = E // G
+    route = route_permute(logits, k, renormalize=renormalize, shared=shared)
+    send, send_counts, s2s = ep_dispatch(x, route, E, k, shared, G, rank, gs_a1)
+    recv_counts = ep_exchange_counts(send_counts, group)
+    # the split sizes are needed on the host (one small device-to-host copy)
+    send_splits = send_counts.sum(dim=1).tolist()
+    recv_splits = recv_counts.sum(dim=1).tolist()
+    recv = ep_exchange_rows(send, send_splits, recv_splits, group)
+    n_recv = sum(recv_splits)
+    g = ep_receive(recv, recv_counts, El, shared, H, n_recv)
+    y = moe_experts(w_local, g["a1"], n_recv, g["offsets"], g["tile_offsets"],
+                    ep_local_scales(gs_a1, E, G, rank, shared), ep_local_scales(gs_a2, E, G, rank, shared), out_dtype)
+    y_ret = ep_return(y, g["recv_to_grp"])
+    y_back = ep_exchange_rows(y_ret, recv_splits, send_splits, group)
+    return moe_combine(y_back, route["topk_w"], s2s, T, k, shared)

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnvfp4moe.so")
-SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "route_static.cu", "router.cu", "w4a16.cu"]
+SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "route_static.cu", "router.cu", "w4a16.cu", "ep.cu"]
 HEADERS = ["internal.h", "layout.cuh", "ptx.cuh", "quant_block.cuh", "route_topk.cuh", os.path.join("..", "..", "include", "nvfp4moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",

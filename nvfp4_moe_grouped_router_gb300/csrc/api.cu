@@ -586,6 +586,139 @@ nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int64_t a_rows, int64_t lda, 
   return NVF_OK;
 }
 
+size_t nvf_ep_row_bytes(int32_t H) { return H > 0 ? ep_row_bytes(H) : 0; }
+
+size_t nvf_ep_receive_scratch_words(int32_t G, int32_t El) {
+  return G > 0 && El > 0 ? 2 * static_cast<size_t>(G) * (El + 1) : 0;
+}
+
+nvf_status nvf_ep_dispatch(const void* x, int32_t T, int32_t H, int32_t E, int32_t k, int32_t shared, int32_t G,
+                           int32_t rank, const int32_t* expert_offsets, const int32_t* perm_token,
+                           const int32_t* perm_to_src, const float* gs_a1, void* send_rows, int32_t* send_counts,
+                           int32_t* src_to_send, void* stream) {
+  NVF_BEGIN();
+  {
+    nvf_status st = validate_route(T, E, k, shared);
+    if (st != NVF_OK) return st;
+  }
+  NVF_REQUIRE(G >= 1 && G <= 1024 && E % G == 0, "G=%d must be in [1, 1024] and divide E=%d", G, E);
+  NVF_REQUIRE(rank >= 0 && rank < G, "rank=%d out of [0, %d)", rank, G);
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(expert_offsets && gs_a1 && send_counts, "expert_offsets, gs_a1 and send_counts must not be NULL");
+  if (T > 0) {
+    NVF_REQUIRE(x && perm_token && perm_to_src && send_rows && src_to_send,
+                "x, perm_token, perm_to_src, send_rows and src_to_send must not be NULL");
+    NVF_REQUIRE(aligned16(x) && aligned16(send_rows), "x and send_rows must be 16-byte aligned");
+  }
+  EpDispatchArgs a{};
+  a.x = x; a.T = T; a.H = H; a.E = E; a.k = k; a.shared = shared; a.G = G; a.rank = rank;
+  a.offsets = expert_offsets; a.perm_token = perm_token; a.perm_to_src = perm_to_src; a.gs_a1 = gs_a1;
+  a.send = static_cast<uint8_t*>(send_rows); a.row_bytes = static_cast<int32_t>(ep_row_bytes(H));
+  a.send_counts = send_counts; a.src_to_send = src_to_send;
+  NVF_CUDA(launch_ep_dispatch(a, static_cast<cudaStream_t>(stream)), "EP dispatch launch");
+  return NVF_OK;
+}
+
+nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* recv_counts, int32_t G, int32_t El,
+                          int32_t shared, int32_t H, uint8_t* a1, int32_t* local_offsets,
+                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(G >= 1 && G <= 1024 && El >= 1 && (shared == 0 || shared == 1), "G=%d, El=%d, shared=%d out of range",
+              G, El, shared);
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(n_recv >= 0 && n_recv < (int64_t(1) << 31), "n_recv=%lld out of range", (long long)n_recv);
+  NVF_REQUIRE(recv_counts && local_offsets && local_tile_offsets && scratch,
+              "recv_counts, local_offsets, local_tile_offsets and scratch must not be NULL");
+  if (n_recv > 0) {
+    NVF_REQUIRE(recv_rows && a1 && recv_to_grp, "recv_rows, a1 and recv_to_grp must not be NULL");
+    NVF_REQUIRE(aligned16(recv_rows) && aligned16(a1), "recv_rows and a1 must be 16-byte aligned");
+  }
+  NVF_CUDA(launch_ep_receive(static_cast<const uint8_t*>(recv_rows), n_recv, static_cast<int>(ep_row_bytes(H)),
+                             recv_counts, G, El, shared, H, a1, local_offsets, local_tile_offsets, recv_to_grp,
+                             scratch, dev_->err, static_cast<cudaStream_t>(stream)),
+           "EP receive launch");
+  return NVF_OK;
+}
+
+nvf_status nvfp4_moe_experts(const nvf_moe_weights* w, const uint8_t* a1, int64_t a_rows, const int32_t* offsets,
+                             const int32_t* tile_offsets, const float* gs_a1, const float* gs_a2, int32_t out_dtype,
+                             void* y, void* ws, size_t ws_bytes, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(w != nullptr, "weights must not be NULL");
+  NVF_REQUIRE(w->E >= 1 && (w->shared == 0 || w->shared == 1) && w->H > 0 && w->H % 128 == 0 && w->I > 0 &&
+                  w->I % 64 == 0,
+              "weights: E=%d shared=%d H=%d I=%d out of range", w->E, w->shared, w->H, w->I);
+  NVF_REQUIRE(a_rows >= 0 && a_rows < (int64_t(1) << 31), "a_rows=%lld out of range", (long long)a_rows);
+  NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
+  if (a_rows == 0) return NVF_OK;
+  const int32_t Et = w->E + w->shared, H = w->H, I = w->I;
+  NVF_REQUIRE(a1 && offsets && tile_offsets && gs_a1 && gs_a2 && y && ws,
+              "a1, offsets, tile_offsets, gs_a1, gs_a2, y and ws must not be NULL");
+  NVF_REQUIRE(w->w13 && w->gs_w13 && w->w2 && w->gs_w2, "weight pointers must not be NULL");
+  NVF_REQUIRE(aligned16(a1) && aligned16(y) && aligned16(w->w13) && aligned16(w->w2),
+              "a1, y and the weights must be 16-byte aligned");
+  NVF_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "ws must be 256-byte aligned");
+  const size_t need = nvfp4_tiled_bytes(a_rows, Et, I);
+  if (ws_bytes < need) return fail(NVF_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const char* why = nullptr;
+  GemmArgs g1{};
+  g1.a = a1; g1.a_rows = a_rows;
+  g1.b = w->w13; g1.gs_a = gs_a1; g1.gs_b = w->gs_w13;
+  g1.offsets = offsets; g1.tile_offs = tile_offsets; g1.G = Et; g1.N = 2 * I; g1.K = H;
+  g1.small_a = a_rows <= 32;  // no group can hold more rows than the buffer
+  g1.epilogue = EPI_SWIGLU_QUANT; g1.q_codes = static_cast<uint8_t*>(ws); g1.gs_q = gs_a2;
+  g1.err = dev_->err;
+  cudaError_t e = launch_grouped_gemm(g1, s, &why);
+  if (e != cudaSuccess)
+    return fail(NVF_ERR_CUDA, "gate_up GEMM (E'=%d rows=%lld): %s", Et, (long long)a_rows,
+                why ? why : cudaGetErrorString(e));
+  GemmArgs g2{};
+  g2.a = static_cast<uint8_t*>(ws); g2.a_rows = a_rows;
+  g2.b = w->w2; g2.gs_a = gs_a2; g2.gs_b = w->gs_w2;
+  g2.offsets = offsets; g2.tile_offs = tile_offsets; g2.G = Et; g2.N = H; g2.K = I;
+  g2.small_a = a_rows <= 32;
+  g2.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
+  g2.d = y; g2.ldd = H; g2.err = dev_->err;
+  g2.d_align32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
+  e = launch_grouped_gemm(g2, s, &why);
+  if (e != cudaSuccess)
+    return fail(NVF_ERR_CUDA, "down GEMM (E'=%d rows=%lld): %s", Et, (long long)a_rows,
+                why ? why : cudaGetErrorString(e));
+  return NVF_OK;
+}
+
+nvf_status nvf_ep_return(const void* y, int64_t n_recv, int32_t H, int32_t dtype, const int32_t* recv_to_grp,
+                         void* y_ret, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(dtype == NVF_F32 || dtype == NVF_BF16, "dtype=%d must be NVF_F32 or NVF_BF16", dtype);
+  NVF_REQUIRE(n_recv >= 0 && n_recv < (int64_t(1) << 31), "n_recv=%lld out of range", (long long)n_recv);
+  if (n_recv == 0) return NVF_OK;
+  NVF_REQUIRE(y && recv_to_grp && y_ret, "y, recv_to_grp and y_ret must not be NULL");
+  NVF_REQUIRE(aligned16(y) && aligned16(y_ret), "y and y_ret must be 16-byte aligned");
+  NVF_CUDA(launch_gather_rows(y, n_recv, static_cast<int64_t>(H) * (dtype == NVF_F32 ? 4 : 2), recv_to_grp, y_ret,
+                              static_cast<cudaStream_t>(stream)),
+           "EP return launch");
+  return NVF_OK;
+}
+
+nvf_status nvf_moe_combine(const void* y, int32_t H, int32_t dtype, const float* topk_w, const int32_t* src_to_row,
+                           int32_t T, int32_t k, int32_t shared, void* out, void* stream) {
+  NVF_BEGIN();
+  NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
+  NVF_REQUIRE(dtype == NVF_F32 || dtype == NVF_BF16, "dtype=%d must be NVF_F32 or NVF_BF16", dtype);
+  NVF_REQUIRE(T >= 0 && k >= 1 && k <= 64 && (shared == 0 || shared == 1), "T=%d k=%d shared=%d out of range", T, k,
+              shared);
+  if (T == 0) return NVF_OK;
+  NVF_REQUIRE(y && topk_w && src_to_row && out, "y, topk_w, src_to_row and out must not be NULL");
+  NVF_REQUIRE((reinterpret_cast<uintptr_t>(y) & 31u) == 0 && aligned16(out), "y must be 32-byte and out 16-byte aligned");
+  NVF_CUDA(launch_combine(y, H, topk_w, src_to_row, T, k, shared, dtype == NVF_BF16 ? X_BF16 : X_F32, out,
+                          static_cast<cudaStream_t>(stream), false),
+           "combine launch");
+  return NVF_OK;
+}
+
 nvf_status nvf_router_gemm(const void* x, const void* w_gate, int32_t T, int32_t H, int32_t n, float* logits,
                            int64_t ldl, void* stream) {
   NVF_BEGIN();

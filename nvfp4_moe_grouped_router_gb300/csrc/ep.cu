@@ -1,0 +1,236 @@
+// Expert-parallel dispatch and return on one rank (the data movement around
+// the all-to-all of the pages' DeepEP prepare/finalize: vLLM PR #35737, CI
+// failure logs, `all2all_manager.get_handle` and the `deepep_high_throughput`
+// MoE prepare/finalize).  Rank `rank` of G owns routed experts
+// [rank El, (rank+1) El), El = E / G; a shared expert is replicated and stays
+// on its rank.  The exchange itself is the caller's collective; these kernels
+// produce and consume its buffers:
+//
+//   dispatch   permuted row p (routing's stable order: by expert, then
+//              assignment) of expert e goes to rank e / El, so the rows for
+//              each rank are one slice of the permutation; a rank's own
+//              segment ends with its shared rows.  Each row is quantized
+//              (NVFP4 with the expert's activation global scale, the block
+//              quantizer of the fused routing kernel) into a send row of
+//              H/2 code bytes then H/16 scale bytes (padded to 16 bytes), at
+//              its send position; src_to_send[a] records where assignment a
+//              went, and send_counts[r][j] the rows for local expert j of
+//              rank r (column El: the shared expert, own rank only).
+//   receive    the arriving rows (sources back to back, each source's rows by
+//              local expert) are grouped by local expert, source by source,
+//              into the grouped GEMM's TILED_GROUPED A operand;
+//              recv_to_grp[i] is received row i's grouped row.
+//   return     y rows, grouped order -> received order, so that the return
+//              exchange delivers each sender its rows at their send
+//              positions, and the combine reads them through src_to_send.
+#include "internal.h"
+#include "layout.cuh"
+#include "ptx.cuh"
+#include "quant_block.cuh"
+
+#include <cuda_bf16.h>
+
+namespace nvf {
+namespace {
+
+constexpr int kEpMaxRanks = 1024;
+
+// One warp per permuted row, 4 rows a CTA.
+__global__ void __launch_bounds__(128) ep_dispatch_kernel(EpDispatchArgs a) {
+  __shared__ int64_t send_off[kEpMaxRanks + 1];
+  const int El = a.E / a.G, Et = a.E + a.shared;
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    for (int r = 0; r < a.G; ++r) {
+      send_off[r] = acc;
+      acc += __ldg(a.offsets + (r + 1) * El) - __ldg(a.offsets + r * El);
+      if (r == a.rank && a.shared) acc += __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+    }
+    send_off[a.G] = acc;
+  }
+  if (blockIdx.x == 0) {
+    for (int c = threadIdx.x; c < a.G * (El + 1); c += blockDim.x) {
+      const int r = c / (El + 1), j = c - r * (El + 1);
+      int n = 0;
+      if (j < El) n = __ldg(a.offsets + r * El + j + 1) - __ldg(a.offsets + r * El + j);
+      else if (r == a.rank && a.shared) n = __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+      a.send_counts[c] = n;
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int64_t R = __ldg(a.offsets + Et);
+  if (p >= R) return;
+  const int e = upper_group(a.offsets, Et, p);
+  int64_t pos;
+  if (e < a.E) {
+    const int dest = e / El;
+    pos = send_off[dest] + (p - __ldg(a.offsets + dest * El));
+  } else {
+    const int64_t own_routed = __ldg(a.offsets + (a.rank + 1) * El) - __ldg(a.offsets + a.rank * El);
+    pos = send_off[a.rank] + own_routed + (p - __ldg(a.offsets + a.E));
+  }
+  const int t = __ldg(a.perm_token + p);
+  if (lane == 0) a.src_to_send[__ldg(a.perm_to_src + p)] = static_cast<int32_t>(pos);
+  const float gs = __ldg(a.gs_a1 + e);
+  const float six_gs = __fmul_rn(6.0f, gs);
+  const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + static_cast<int64_t>(t) * a.H);
+  uint8_t* row = a.send + pos * static_cast<int64_t>(a.row_bytes);
+  for (int b = lane; b < a.H / 16; b += 32) {
+    const uint4 u0 = __ldg(xr + 2 * b), u1 = __ldg(xr + 2 * b + 1);
+    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(wv[i] << 16);               // bf16 -> fp32 is exact
+      v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+    }
+    uint32_t w0, w1;
+    const uint32_t sb = quant_block16(v, gs, six_gs, w0, w1);
+    *reinterpret_cast<uint2*>(row + b * 8) = make_uint2(w0, w1);
+    row[a.H / 2 + b] = static_cast<uint8_t>(sb);
+  }
+}
+
+// One CTA: local offsets, tile offsets and, per (source s, local expert j)
+// cell c = s * J + j, the cell's first received row (recv_base) and first
+// grouped row (grp_base).  J = El + 1 count columns; Et_l = El + shared local
+// experts.
+__global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __restrict__ counts, int G, int El,
+                                                              int shared, int32_t* local_offsets,
+                                                              int32_t* local_tile_offsets, int32_t* recv_base,
+                                                              int32_t* grp_base) {
+  const int J = El + 1, Et_l = El + shared, cells = G * J;
+  __shared__ int32_t s_off[2];
+  __shared__ int32_t part[256];
+  // expert totals and their prefixes (one thread: Et_l <= a few thousand)
+  if (threadIdx.x == 0) {
+    int32_t off = 0, toff = 0;
+    for (int j = 0; j < Et_l; ++j) {
+      local_offsets[j] = off;
+      local_tile_offsets[j] = toff;
+      int32_t n = 0;
+      for (int s = 0; s < G; ++s) n += __ldg(counts + s * J + j);
+      off += n;
+      toff += (n + 127) / 128;
+    }
+    local_offsets[Et_l] = off;
+    local_tile_offsets[Et_l] = toff;
+    s_off[0] = off;
+  }
+  __syncthreads();
+  // grp_base: per expert column, the sources' running sum
+  for (int j = threadIdx.x; j < J; j += blockDim.x) {
+    int32_t acc = j < Et_l ? local_offsets[j] : s_off[0];
+    for (int s = 0; s < G; ++s) {
+      grp_base[s * J + j] = acc;
+      acc += __ldg(counts + s * J + j);
+    }
+  }
+  // recv_base: exclusive prefix over the cells in (s, j) order, chunk per thread
+  const int per = (cells + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(cells, static_cast<int>(threadIdx.x) * per), c1 = min(cells, c0 + per);
+  int32_t sum = 0;
+  for (int c = c0; c < c1; ++c) sum += __ldg(counts + c);
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t acc = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
+      const int32_t v = part[i];
+      part[i] = acc;
+      acc += v;
+    }
+  }
+  __syncthreads();
+  int32_t acc = part[threadIdx.x];
+  for (int c = c0; c < c1; ++c) {
+    recv_base[c] = acc;
+    acc += __ldg(counts + c);
+  }
+}
+
+// One warp per received row, 4 rows a CTA.
+__global__ void __launch_bounds__(128) ep_receive_scatter_kernel(const uint8_t* __restrict__ recv, int64_t n_recv,
+                                                                 int row_bytes, int H, int G, int El,
+                                                                 const int32_t* __restrict__ local_offsets,
+                                                                 const int32_t* __restrict__ local_tile_offsets,
+                                                                 const int32_t* __restrict__ recv_base,
+                                                                 const int32_t* __restrict__ grp_base,
+                                                                 const int32_t* __restrict__ counts, uint8_t* a1,
+                                                                 int32_t* recv_to_grp, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (i >= n_recv) return;
+  const int J = El + 1;
+  const int c = upper_group(recv_base, G * J, i);      // the (source, expert) cell holding row i
+  if (i - __ldg(recv_base + c) >= __ldg(counts + c)) {  // more rows than the counts hold: stay in bounds
+    if (lane == 0) report_error(err, DEV_BAD_OFFSETS, static_cast<int>(i));
+    return;
+  }
+  const int j = c % J;
+  const int32_t g = __ldg(grp_base + c) + static_cast<int32_t>(i - __ldg(recv_base + c));
+  const int32_t local = g - __ldg(local_offsets + j);
+  const int64_t tile = __ldg(local_tile_offsets + j) + (local >> 7);
+  const uint32_t r = static_cast<uint32_t>(local & 127);
+  if (lane == 0) recv_to_grp[i] = g;
+  const uint8_t* row = recv + i * static_cast<int64_t>(row_bytes);
+  for (int gg = lane; gg < H / 64; gg += 32) {
+    const uint4 u0 = *reinterpret_cast<const uint4*>(row + gg * 32);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(row + gg * 32 + 16);
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const uint32_t sf = *reinterpret_cast<const uint32_t*>(row + H / 2 + gg * 4);
+    store_group64(a1, nullptr, LAYOUT_TILED_GROUPED, H, g, tile, r, gg, w, sf);
+  }
+}
+
+// out row i = in row idx[i]; 16 bytes a thread.
+__global__ void ep_gather_rows_kernel(const uint4* __restrict__ in, int64_t n, int row_units,
+                                      const int32_t* __restrict__ idx, uint4* out) {
+  const int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q >= n * row_units) return;
+  const int64_t i = q / row_units;
+  const int u = static_cast<int>(q - i * row_units);
+  out[q] = in[static_cast<int64_t>(__ldg(idx + i)) * row_units + u];
+}
+
+}  // namespace
+
+size_t ep_row_bytes(int H) { return (static_cast<size_t>(H) / 2 + static_cast<size_t>(H) / 16 + 15) & ~size_t(15); }
+
+cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s) {
+  if (a.G > kEpMaxRanks) return cudaErrorInvalidValue;
+  const int64_t R = static_cast<int64_t>(a.T) * a.k + (a.shared ? a.T : 0);
+  const int64_t blocks = R > 0 ? (R + 3) / 4 : 1;     // one CTA at least: it writes send_counts
+  ep_dispatch_kernel<<<static_cast<unsigned>(blocks), 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes, const int32_t* counts, int G,
+                              int El, int shared, int H, uint8_t* a1, int32_t* local_offsets,
+                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, int* err,
+                              cudaStream_t s) {
+  int32_t* recv_base = scratch;
+  int32_t* grp_base = scratch + static_cast<int64_t>(G) * (El + 1);
+  ep_receive_plan_kernel<<<1, 256, 0, s>>>(counts, G, El, shared, local_offsets, local_tile_offsets, recv_base,
+                                            grp_base);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || n_recv == 0) return e;
+  ep_receive_scatter_kernel<<<static_cast<unsigned>((n_recv + 3) / 4), 128, 0, s>>>(
+      recv, n_recv, row_bytes, H, G, El, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
+      recv_to_grp, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* in, int64_t n, int64_t row_bytes, const int32_t* idx, void* out,
+                               cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int units = static_cast<int>(row_bytes / 16);
+  const int64_t total = n * units;
+  ep_gather_rows_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+      static_cast<const uint4*>(in), n, units, idx, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace nvf

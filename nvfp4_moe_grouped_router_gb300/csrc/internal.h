@@ -127,6 +127,28 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s, const char** why);
 
 int* device_error_word();   // per current device, nullptr on failure
+// Expert-parallel dispatch / receive / return (ep.cu).
+struct EpDispatchArgs {
+  const void* x;                  // bf16 [T, H]
+  int32_t T, H, E, k, shared, G, rank;
+  const int32_t* offsets;         // routing's expert offsets [E + shared + 1]
+  const int32_t* perm_token;      // [R]
+  const int32_t* perm_to_src;     // [R]
+  const float* gs_a1;             // [E + shared], global expert ids
+  uint8_t* send;                  // [R, row_bytes]
+  int32_t row_bytes;
+  int32_t* send_counts;           // [G, E/G + 1]
+  int32_t* src_to_send;           // [R]
+};
+size_t ep_row_bytes(int H);
+cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s);
+cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes, const int32_t* counts, int G,
+                              int El, int shared, int H, uint8_t* a1, int32_t* local_offsets,
+                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, int* err,
+                              cudaStream_t s);
+cudaError_t launch_gather_rows(const void* in, int64_t n, int64_t row_bytes, const int32_t* idx, void* out,
+                               cudaStream_t s);
+
 int sm_count();
 // Ask for the largest shared-memory carveout once per (device, kernel), so that
 // consecutive kernels of the layer do not reconfigure L1 / shared memory.
