@@ -474,6 +474,79 @@ def w4a16_sweep(args):
                           "hbm_frac": gbs / hbm, "peak_source": src, "steps": n}), flush=True)
 
 
+def ep_sweep(args):
+    """Expert parallelism over G ranks, emulated on one GPU: every rank holds
+    the workload's batch (seeded per rank), routes it over all experts and
+    dispatches; rank 0 receives its segment of every rank's rows, runs its
+    E/G experts, returns the rows and combines what comes back.  The exchanges
+    are tensor slices here; their bytes are reported.  One JSON line per
+    workload: rank 0's device time per step (each a CUDA graph of calls) next
+    to the single-device forward of the same batch (all experts local)."""
+    import nvfp4_moe_grouped_router_gb300 as nvf
+    from nvfp4_moe_grouped_router_gb300 import build as nvf_build
+    torch.cuda.set_device(0)
+    nvf_build.build()
+    nvf.lib()
+    G = args.ep
+    steps = max(3, min(args.steps, 200))
+    for name in ("decode", "prefill"):
+        cfg = CONFIGS[name]
+        El, H = cfg.E // G, cfg.H
+        gs1, gs2 = activation_scales(cfg.name)
+        gs_a1 = torch.full((cfg.E_total,), gs1, device="cuda")
+        gs_a2 = torch.full((cfg.E_total,), gs2, device="cuda")
+        xs, routes, sends = [], [], []
+        for r in range(G):
+            x, lg, _ = make_inputs(cfg, 1000 + r, device="cpu")
+            x, lg = x.cuda(), lg.cuda()
+            route = nvf.route_permute(lg, cfg.k, renormalize=cfg.renormalize, shared=cfg.shared)
+            xs.append(x)
+            routes.append(route)
+            sends.append(nvf.ep_dispatch(x, route, cfg.E, cfg.k, cfg.shared, G, r, gs_a1))
+        bounds = [np.concatenate([[0], np.cumsum(c.sum(dim=1).cpu().numpy())]) for _, c, _ in sends]
+        recv = torch.cat([sends[s][0][bounds[s][0]:bounds[s][1]] for s in range(G)])
+        rc = torch.stack([sends[s][1][0] for s in range(G)]).contiguous()
+        n = int(rc.sum().item())
+        tail = [cfg.E] if cfg.shared else []
+        ids = list(range(El)) + tail
+        w0 = nvf.prepare_weights(El, H, cfg.I, cfg.shared, lambda j: expert_weights(cfg, ids[j], 0, device="cuda"))
+        g = nvf.ep_receive(recv, rc, El, cfg.shared, H, n)
+        l1 = nvf.ep_local_scales(gs_a1, cfg.E, G, 0, cfg.shared)
+        l2 = nvf.ep_local_scales(gs_a2, cfg.E, G, 0, cfg.shared)
+        y = nvf.moe_experts(w0, g["a1"], n, g["offsets"], g["tile_offsets"], l1, l2, torch.bfloat16)
+        R = sends[0][2].numel()
+        y_back = torch.zeros(R, H, dtype=torch.bfloat16, device="cuda")
+        t = {
+            "dispatch": _graph_time_us(lambda i: nvf.ep_dispatch(xs[0], routes[0], cfg.E, cfg.k, cfg.shared, G, 0,
+                                                                 gs_a1), steps, args.warmup),
+            "receive": _graph_time_us(lambda i: nvf.ep_receive(recv, rc, El, cfg.shared, H, n), steps, args.warmup),
+            "experts": _graph_time_us(lambda i: nvf.moe_experts(w0, g["a1"], n, g["offsets"], g["tile_offsets"], l1,
+                                                                l2, torch.bfloat16), steps, args.warmup),
+            "return": _graph_time_us(lambda i: nvf.ep_return(y, g["recv_to_grp"]), steps, args.warmup),
+            "combine": _graph_time_us(lambda i: nvf.moe_combine(y_back, routes[0]["topk_w"], sends[0][2], cfg.T,
+                                                                cfg.k, cfg.shared), steps, args.warmup),
+        }
+        del w0
+        wf = nvf.prepare_weights(cfg.E, H, cfg.I, cfg.shared, lambda e: expert_weights(cfg, e, 0, device="cuda"))
+        lg0 = make_inputs(cfg, 1000, device="cpu")[1].cuda()
+        ws = nvf.workspace(cfg.T, wf, cfg.k)
+        out = torch.empty(cfg.T, H, dtype=torch.bfloat16, device="cuda")
+        single = _graph_time_us(lambda i: nvf.moe_forward(wf, xs[0], lg0, cfg.k, gs_a1, gs_a2,
+                                                          renormalize=cfg.renormalize, out=out, ws=ws),
+                                steps, args.warmup)
+        del wf
+        code, detail = nvf.device_status()
+        if code != 0:
+            raise RuntimeError(f"device error word {code} at {detail}")
+        row_bytes = nvf.ep_row_bytes(H)
+        print(json.dumps({"metric": f"expert parallelism over {G} ranks, emulated on one GPU: rank 0 device us per step",
+                          "workload": name, "G": G, "tokens_per_rank": cfg.T, "rows_sent": R, "rows_received": n,
+                          "us": {k: round(v, 2) for k, v in t.items()}, "us_total": round(sum(t.values()), 2),
+                          "single_device_forward_us": round(single, 2),
+                          "exchange_bytes_per_rank": {"dispatch": int(R * row_bytes), "return": int(R * H * 2)},
+                          "exchange": "not timed (one GPU)", "steps": steps, "data": "synthetic"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,7 +561,10 @@ def main():
                     help="the dense W4A4 linear sweep (N=34816, K=5120, M=1..4096) instead of the MoE layer")
     ap.add_argument("--router", action="store_true", help="the router gate GEMM at the decode and prefill batches")
     ap.add_argument("--w4a16", action="store_true", help="the weight-only (W4A16) GEMM beside W4A4")
+    ap.add_argument("--ep", type=int, default=0, help="expert parallelism over this many ranks, emulated on one GPU")
     args = ap.parse_args()
+    if args.ep:
+        return ep_sweep(args)
     if args.w4a16:
         return w4a16_sweep(args)
     if args.dense:

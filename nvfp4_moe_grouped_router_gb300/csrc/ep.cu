@@ -93,58 +93,86 @@ __global__ void __launch_bounds__(128) ep_dispatch_kernel(EpDispatchArgs a) {
   }
 }
 
-// One CTA: local offsets, tile offsets and, per (source s, local expert j)
-// cell c = s * J + j, the cell's first received row (recv_base) and first
-// grouped row (grp_base).  J = El + 1 count columns; Et_l = El + shared local
-// experts.
+// Exclusive prefix sum over the 256 threads of the block (warp shuffles, then
+// the warps' totals); *total gets the sum.  Every thread must call it.
+__device__ __forceinline__ int32_t block_scan_excl(int32_t v, int32_t* warp_sums, int32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int32_t base = warp > 0 ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[nw - 1];
+  __syncthreads();                                       // warp_sums is reused by the next scan
+  return base + x - v;
+}
+
+// One CTA of 256 threads: local offsets, tile offsets and, per (source s, local
+// expert j) cell c = s * J + j, the cell's first received row (recv_base) and
+// first grouped row (grp_base).  J = El + 1 count columns; Et_l = El + shared
+// local experts.  Thread t handles a contiguous chunk of experts, then of cells.
 __global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __restrict__ counts, int G, int El,
                                                               int shared, int32_t* local_offsets,
                                                               int32_t* local_tile_offsets, int32_t* recv_base,
                                                               int32_t* grp_base) {
   const int J = El + 1, Et_l = El + shared, cells = G * J;
-  __shared__ int32_t s_off[2];
-  __shared__ int32_t part[256];
-  // expert totals and their prefixes (one thread: Et_l <= a few thousand)
-  if (threadIdx.x == 0) {
-    int32_t off = 0, toff = 0;
-    for (int j = 0; j < Et_l; ++j) {
+  __shared__ int32_t warp_sums[32];
+  // experts [j0, j1) of this thread: totals over the sources, then the prefix
+  const int per_e = (J + blockDim.x - 1) / blockDim.x;
+  const int j0 = min(J, static_cast<int>(threadIdx.x) * per_e), j1 = min(J, j0 + per_e);
+  int32_t rows = 0, tiles = 0;
+  for (int j = j0; j < min(j1, Et_l); ++j) {
+    int32_t n = 0;
+    for (int s = 0; s < G; ++s) n += __ldg(counts + s * J + j);
+    rows += n;
+    tiles += (n + 127) / 128;
+  }
+  int32_t total_rows, total_tiles;
+  int32_t off = block_scan_excl(rows, warp_sums, &total_rows);
+  int32_t toff = block_scan_excl(tiles, warp_sums, &total_tiles);
+  for (int j = j0; j < j1; ++j) {
+    int32_t n = 0;
+    if (j < Et_l) {
       local_offsets[j] = off;
       local_tile_offsets[j] = toff;
-      int32_t n = 0;
-      for (int s = 0; s < G; ++s) n += __ldg(counts + s * J + j);
+    }
+    int32_t acc = j < Et_l ? off : total_rows;           // the shared column of a layer without one is empty
+    for (int s = 0; s < G; ++s) {
+      grp_base[s * J + j] = acc;
+      const int32_t c = __ldg(counts + s * J + j);
+      acc += c;
+      n += c;
+    }
+    if (j < Et_l) {
       off += n;
       toff += (n + 127) / 128;
     }
-    local_offsets[Et_l] = off;
-    local_tile_offsets[Et_l] = toff;
-    s_off[0] = off;
   }
-  __syncthreads();
-  // grp_base: per expert column, the sources' running sum
-  for (int j = threadIdx.x; j < J; j += blockDim.x) {
-    int32_t acc = j < Et_l ? local_offsets[j] : s_off[0];
-    for (int s = 0; s < G; ++s) {
-      grp_base[s * J + j] = acc;
-      acc += __ldg(counts + s * J + j);
-    }
+  if (threadIdx.x == 0) {
+    local_offsets[Et_l] = total_rows;
+    local_tile_offsets[Et_l] = total_tiles;
   }
-  // recv_base: exclusive prefix over the cells in (s, j) order, chunk per thread
+  // recv_base: exclusive prefix over the cells in (s, j) order
   const int per = (cells + blockDim.x - 1) / blockDim.x;
   const int c0 = min(cells, static_cast<int>(threadIdx.x) * per), c1 = min(cells, c0 + per);
   int32_t sum = 0;
   for (int c = c0; c < c1; ++c) sum += __ldg(counts + c);
-  part[threadIdx.x] = sum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t acc = 0;
-    for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
-      const int32_t v = part[i];
-      part[i] = acc;
-      acc += v;
-    }
-  }
-  __syncthreads();
-  int32_t acc = part[threadIdx.x];
+  int32_t total_cells;
+  int32_t acc = block_scan_excl(sum, warp_sums, &total_cells);
   for (int c = c0; c < c1; ++c) {
     recv_base[c] = acc;
     acc += __ldg(counts + c);
