@@ -520,9 +520,10 @@ def ep_sweep(args):
             "dispatch": _graph_time_us(lambda i: nvf.ep_dispatch(xs[0], routes[0], cfg.E, cfg.k, cfg.shared, G, 0,
                                                                  gs_a1), steps, args.warmup),
             "receive": _graph_time_us(lambda i: nvf.ep_receive(recv, rc, El, cfg.shared, H, n), steps, args.warmup),
+            # the down GEMM stores y in received order (row map): no separate return kernel
             "experts": _graph_time_us(lambda i: nvf.moe_experts(w0, g["a1"], n, g["offsets"], g["tile_offsets"], l1,
-                                                                l2, torch.bfloat16), steps, args.warmup),
-            "return": _graph_time_us(lambda i: nvf.ep_return(y, g["recv_to_grp"]), steps, args.warmup),
+                                                                l2, torch.bfloat16, y_rows=g["grp_to_recv"]),
+                                      steps, args.warmup),
             "combine": _graph_time_us(lambda i: nvf.moe_combine(y_back, routes[0]["topk_w"], sends[0][2], cfg.T,
                                                                 cfg.k, cfg.shared), steps, args.warmup),
         }
@@ -542,6 +543,8 @@ def ep_sweep(args):
         print(json.dumps({"metric": f"expert parallelism over {G} ranks, emulated on one GPU: rank 0 device us per step",
                           "workload": name, "G": G, "tokens_per_rank": cfg.T, "rows_sent": R, "rows_received": n,
                           "us": {k: round(v, 2) for k, v in t.items()}, "us_total": round(sum(t.values()), 2),
+                          "separate_return_kernel_us": round(_graph_time_us(
+                              lambda i: nvf.ep_return(y, g["recv_to_grp"]), steps, args.warmup), 2),
                           "single_device_forward_us": round(single, 2),
                           "exchange_bytes_per_rank": {"dispatch": int(R * row_bytes), "return": int(R * H * 2)},
                           "exchange": "not timed (one GPU)", "steps": steps, "data": "synthetic"}), flush=True)

@@ -406,11 +406,13 @@ size_t nvf_ep_receive_scratch_words(int32_t G, int32_t El);
  * NVF_LAYOUT_TILED_GROUPED (nvfp4_tiled_bytes(n_recv, El + shared, H) bytes,
  * 16-byte aligned); local_offsets and local_tile_offsets int32
  * [El + shared + 1] (local expert j's rows: source 0's, then source 1's, ...);
- * recv_to_grp int32 [n_recv], received row i's grouped row.  scratch: device
- * int32 [nvf_ep_receive_scratch_words(G, El)]. */
+ * recv_to_grp int32 [n_recv], received row i's grouped row; grp_to_recv
+ * (nullable) int32 [n_recv], its inverse.  scratch: device int32
+ * [nvf_ep_receive_scratch_words(G, El)]. */
 nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* recv_counts, int32_t G, int32_t El,
                           int32_t shared, int32_t H, uint8_t* a1, int32_t* local_offsets,
-                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, void* stream);
+                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* grp_to_recv, int32_t* scratch,
+                          void* stream);
 
 /* The expert computation of steps 4-6 on grouped rows (the layer's GEMMs
  * without routing): y[p] = alpha2_e * A2_p . W2_e^T with A2 the NVFP4 of
@@ -419,11 +421,14 @@ nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* 
  * NVF_LAYOUT_TILED_GROUPED [a_rows, H] rows grouped by offsets / tile_offsets
  * (int32 [E + shared + 1], device); gs_a1, gs_a2: device float [E + shared];
  * y: device [a_rows, H] of out_dtype (NVF_F32 | NVF_BF16), 16-byte aligned;
- * ws: device scratch of nvfp4_tiled_bytes(a_rows, E + shared, I) bytes
- * (the A2 operand), 256-byte aligned. */
+ * y_rows: nullable device int32 [a_rows], a permutation of [0, a_rows): grouped
+ * row p is stored as y row y_rows[p] (with nvf_ep_receive's grp_to_recv, y
+ * comes out in received order and nvf_ep_return is not needed); NULL stores
+ * row p as row p.  ws: device scratch of nvfp4_tiled_bytes(a_rows, E + shared,
+ * I) bytes (the A2 operand), 256-byte aligned. */
 nvf_status nvfp4_moe_experts(const nvf_moe_weights* w, const uint8_t* a1, int64_t a_rows, const int32_t* offsets,
                              const int32_t* tile_offsets, const float* gs_a1, const float* gs_a2, int32_t out_dtype,
-                             void* y, void* ws, size_t ws_bytes, void* stream);
+                             void* y, const int32_t* y_rows, void* ws, size_t ws_bytes, void* stream);
 
 /* Return: y_ret[i] = y[recv_to_grp[i]] (rows of H elements of dtype NVF_F32 or
  * NVF_BF16, device, 16-byte aligned), the received order, which the return

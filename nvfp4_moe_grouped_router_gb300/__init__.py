@@ -53,8 +53,8 @@ SIGNATURES = {
     "nvf_ep_receive_scratch_words": (_SZ, [_I32, _I32]),
     "nvf_ep_dispatch": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P]),
-    "nvf_ep_receive": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
-    "nvfp4_moe_experts": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "nvf_ep_receive": (ctypes.c_int, [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "nvfp4_moe_experts": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "nvf_ep_return": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P]),
     "nvf_moe_combine": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _P]),
 }
@@ -380,21 +380,24 @@ def ep_receive(recv_rows, recv_counts, El: int, shared: bool, H: int, n_recv: in
     off = torch.empty(Et + 1, dtype=torch.int32, device=dev)
     toff = torch.empty(Et + 1, dtype=torch.int32, device=dev)
     r2g = torch.empty(max(n_recv, 1), dtype=torch.int32, device=dev)
+    g2r = torch.empty(max(n_recv, 1), dtype=torch.int32, device=dev)
     scratch = torch.empty(int(lib().nvf_ep_receive_scratch_words(G, El)), dtype=torch.int32, device=dev)
     _check(lib().nvf_ep_receive(_ptr(recv_rows), n_recv, _ptr(recv_counts), G, El, int(shared), H, _ptr(a1), _ptr(off),
-                                _ptr(toff), _ptr(r2g), _ptr(scratch), _stream()))
-    return dict(a1=a1, offsets=off, tile_offsets=toff, recv_to_grp=r2g[:n_recv], n=n_recv)
+                                _ptr(toff), _ptr(r2g), _ptr(g2r), _ptr(scratch), _stream()))
+    return dict(a1=a1, offsets=off, tile_offsets=toff, recv_to_grp=r2g[:n_recv], grp_to_recv=g2r[:n_recv], n=n_recv)
 
 
-def moe_experts(w: MoEWeights, a1, a_rows: int, offsets, tile_offsets, gs_a1, gs_a2, out_dtype=torch.float32):
-    """Steps 4-6 on grouped rows: y [a_rows, H]."""
+def moe_experts(w: MoEWeights, a1, a_rows: int, offsets, tile_offsets, gs_a1, gs_a2, out_dtype=torch.float32,
+                y_rows=None):
+    """Steps 4-6 on grouped rows: y [a_rows, H]; with y_rows, grouped row p is
+    stored as y row y_rows[p]."""
     dev = a1.device
     y = torch.empty(max(a_rows, 1), w.H, dtype=out_dtype, device=dev)
     ws = torch.empty(max(tiled_bytes(a_rows, w.E + int(w.shared), w.I), 256), dtype=torch.uint8, device=dev)
     cw = w.c_struct()
     _check(lib().nvfp4_moe_experts(ctypes.byref(cw), _ptr(a1), a_rows, _ptr(offsets), _ptr(tile_offsets), _ptr(gs_a1),
-                                   _ptr(gs_a2), NVF_F32 if out_dtype == torch.float32 else NVF_BF16, _ptr(y), _ptr(ws),
-                                   ws.numel(), _stream()))
+                                   _ptr(gs_a2), NVF_F32 if out_dtype == torch.float32 else NVF_BF16, _ptr(y),
+                                   _ptr(y_rows), _ptr(ws), ws.numel(), _stream()))
     return y[:a_rows]
 
 
@@ -460,8 +463,9 @@ def ep_forward(w_local: MoEWeights, x, logits, k: int, E: int, gs_a1, gs_a2, sha
     recv = ep_exchange_rows(send, send_splits, recv_splits, group)
     n_recv = sum(recv_splits)
     g = ep_receive(recv, recv_counts, El, shared, H, n_recv)
-    y = moe_experts(w_local, g["a1"], n_recv, g["offsets"], g["tile_offsets"],
-                    ep_local_scales(gs_a1, E, G, rank, shared), ep_local_scales(gs_a2, E, G, rank, shared), out_dtype)
-    y_ret = ep_return(y, g["recv_to_grp"])
+    # the down GEMM stores y rows in received order: the return exchange sends them as they are
+    y_ret = moe_experts(w_local, g["a1"], n_recv, g["offsets"], g["tile_offsets"],
+                        ep_local_scales(gs_a1, E, G, rank, shared), ep_local_scales(gs_a2, E, G, rank, shared),
+                        out_dtype, y_rows=g["grp_to_recv"])
     y_back = ep_exchange_rows(y_ret, recv_splits, send_splits, group)
     return moe_combine(y_back, route["topk_w"], s2s, T, k, shared)

@@ -621,7 +621,8 @@ nvf_status nvf_ep_dispatch(const void* x, int32_t T, int32_t H, int32_t E, int32
 
 nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* recv_counts, int32_t G, int32_t El,
                           int32_t shared, int32_t H, uint8_t* a1, int32_t* local_offsets,
-                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, void* stream) {
+                          int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* grp_to_recv, int32_t* scratch,
+                          void* stream) {
   NVF_BEGIN();
   NVF_REQUIRE(G >= 1 && G <= 1024 && El >= 1 && (shared == 0 || shared == 1), "G=%d, El=%d, shared=%d out of range",
               G, El, shared);
@@ -635,14 +636,14 @@ nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* 
   }
   NVF_CUDA(launch_ep_receive(static_cast<const uint8_t*>(recv_rows), n_recv, static_cast<int>(ep_row_bytes(H)),
                              recv_counts, G, El, shared, H, a1, local_offsets, local_tile_offsets, recv_to_grp,
-                             scratch, dev_->err, static_cast<cudaStream_t>(stream)),
+                             grp_to_recv, scratch, dev_->err, static_cast<cudaStream_t>(stream)),
            "EP receive launch");
   return NVF_OK;
 }
 
 nvf_status nvfp4_moe_experts(const nvf_moe_weights* w, const uint8_t* a1, int64_t a_rows, const int32_t* offsets,
                              const int32_t* tile_offsets, const float* gs_a1, const float* gs_a2, int32_t out_dtype,
-                             void* y, void* ws, size_t ws_bytes, void* stream) {
+                             void* y, const int32_t* y_rows, void* ws, size_t ws_bytes, void* stream) {
   NVF_BEGIN();
   NVF_REQUIRE(w != nullptr, "weights must not be NULL");
   NVF_REQUIRE(w->E >= 1 && (w->shared == 0 || w->shared == 1) && w->H > 0 && w->H % 128 == 0 && w->I > 0 &&
@@ -679,7 +680,7 @@ nvf_status nvfp4_moe_experts(const nvf_moe_weights* w, const uint8_t* a1, int64_
   g2.offsets = offsets; g2.tile_offs = tile_offsets; g2.G = Et; g2.N = H; g2.K = I;
   g2.small_a = a_rows <= 32;
   g2.epilogue = out_dtype == NVF_F32 ? EPI_STORE_F32 : EPI_STORE_BF16;
-  g2.d = y; g2.ldd = H; g2.err = dev_->err;
+  g2.d = y; g2.ldd = H; g2.err = dev_->err; g2.d_rows = y_rows;
   g2.d_align32 = (reinterpret_cast<uintptr_t>(y) & 31u) == 0;
   e = launch_grouped_gemm(g2, s, &why);
   if (e != cudaSuccess)

@@ -19,7 +19,9 @@
 //   receive    the arriving rows (sources back to back, each source's rows by
 //              local expert) are grouped by local expert, source by source,
 //              into the grouped GEMM's TILED_GROUPED A operand;
-//              recv_to_grp[i] is received row i's grouped row.
+//              recv_to_grp[i] is received row i's grouped row, grp_to_recv
+//              its inverse (the down GEMM can store y rows straight in
+//              received order with it).
 //   return     y rows, grouped order -> received order, so that the return
 //              exchange delivers each sender its rows at their send
 //              positions, and the combine reads them through src_to_send.
@@ -187,7 +189,8 @@ __global__ void __launch_bounds__(128) ep_receive_scatter_kernel(const uint8_t* 
                                                                  const int32_t* __restrict__ recv_base,
                                                                  const int32_t* __restrict__ grp_base,
                                                                  const int32_t* __restrict__ counts, uint8_t* a1,
-                                                                 int32_t* recv_to_grp, int* err) {
+                                                                 int32_t* recv_to_grp, int32_t* grp_to_recv,
+                                                                 int* err) {
   const int lane = threadIdx.x & 31;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (i >= n_recv) return;
@@ -202,7 +205,10 @@ __global__ void __launch_bounds__(128) ep_receive_scatter_kernel(const uint8_t* 
   const int32_t local = g - __ldg(local_offsets + j);
   const int64_t tile = __ldg(local_tile_offsets + j) + (local >> 7);
   const uint32_t r = static_cast<uint32_t>(local & 127);
-  if (lane == 0) recv_to_grp[i] = g;
+  if (lane == 0) {
+    recv_to_grp[i] = g;
+    if (grp_to_recv != nullptr) grp_to_recv[g] = static_cast<int32_t>(i);
+  }
   const uint8_t* row = recv + i * static_cast<int64_t>(row_bytes);
   for (int gg = lane; gg < H / 64; gg += 32) {
     const uint4 u0 = *reinterpret_cast<const uint4*>(row + gg * 32);
@@ -237,8 +243,8 @@ cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s) {
 
 cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes, const int32_t* counts, int G,
                               int El, int shared, int H, uint8_t* a1, int32_t* local_offsets,
-                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, int* err,
-                              cudaStream_t s) {
+                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* grp_to_recv,
+                              int32_t* scratch, int* err, cudaStream_t s) {
   int32_t* recv_base = scratch;
   int32_t* grp_base = scratch + static_cast<int64_t>(G) * (El + 1);
   ep_receive_plan_kernel<<<1, 256, 0, s>>>(counts, G, El, shared, local_offsets, local_tile_offsets, recv_base,
@@ -247,7 +253,7 @@ cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes
   if (e != cudaSuccess || n_recv == 0) return e;
   ep_receive_scatter_kernel<<<static_cast<unsigned>((n_recv + 3) / 4), 128, 0, s>>>(
       recv, n_recv, row_bytes, H, G, El, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
-      recv_to_grp, err);
+      recv_to_grp, grp_to_recv, err);
   return cudaGetLastError();
 }
 

@@ -551,6 +551,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
         constexpr int CHUNK_COLS = F32 ? 32 : 64;             // 128 bytes of a row
         const uint32_t stg = s_base + SM::OFF_STG + static_cast<uint32_t>((warp - EPI_WARP0) * SM::STG_WARP_BYTES);
         const int rows_here = min(32, x.rows - q * 32);       // valid rows of this warp's quarter
+        // with a row map, lane l holds the output row of the quarter's row l
+        const int32_t out_row = p.d_rows != nullptr && lane < rows_here
+                                    ? __ldg(p.d_rows + x.row0 + q * 32 + lane) : 0;
 #pragma unroll
         for (int ch = 0; ch < 128 / CHUNK_COLS; ++ch) {
 #pragma unroll
@@ -573,27 +576,29 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
           }
           __syncwarp();
           const int pc = lane & 7;
-          // this lane's first row (lane / 8) and its 16-byte piece of the chunk
+          // this lane's 16-byte piece of the chunk; rows 4 i + lane / 8 of the quarter
           constexpr int ESZ = F32 ? 4 : 2;
           const int64_t pitch = p.ldd * ESZ;
-          uint8_t* dst = static_cast<uint8_t*>(p.d) +
-                         (static_cast<int64_t>(x.row0) + q * 32 + (lane >> 3)) * pitch +
-                         (static_cast<int64_t>(nt) * 128 + ch * CHUNK_COLS) * ESZ + pc * 16;
+          uint8_t* dst = static_cast<uint8_t*>(p.d) + (static_cast<int64_t>(nt) * 128 + ch * CHUNK_COLS) * ESZ + pc * 16;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int rr = 4 * i + (lane >> 3);                 // row within the warp's quarter
             const uint4 d = ld_shared_v4(stg + rr * 128 + ((pc ^ (rr & 7)) * 16));
-            if (rr < rows_here) *reinterpret_cast<uint4*>(dst + 4 * i * pitch) = d;
+            // output row: the grouped row itself, or where the row map sends it
+            const int64_t orow = p.d_rows == nullptr ? static_cast<int64_t>(x.row0) + q * 32 + rr
+                                                     : static_cast<int64_t>(__shfl_sync(0xffffffffu, out_row, rr));
+            if (rr < rows_here) *reinterpret_cast<uint4*>(dst + orow * pitch) = d;
           }
           __syncwarp();
         }
       } else {
         if (!valid) continue;
+        const int64_t orow = p.d_rows == nullptr ? row : static_cast<int64_t>(__ldg(p.d_rows + row));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int64_t col = static_cast<int64_t>(nt) * 128 + c * 32;
           if constexpr (EPI == EPI_STORE_F32) {
-            float* drow = static_cast<float*>(p.d) + row * p.ldd + col;
+            float* drow = static_cast<float*>(p.d) + orow * p.ldd + col;
             if (p.d_align32) {
               // whole 32-byte sectors per instruction
 #pragma unroll
@@ -613,7 +618,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
                                      __fmul_rn(__uint_as_float(v[c][4 * j + 3]), alpha));
             }
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + row * p.ldd + col);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.d) + orow * p.ldd + col);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t w[4];

@@ -112,6 +112,7 @@ struct GemmArgs {
   int epilogue;
   void* d;                  // STORE: [rows, ldd]
   int64_t ldd;
+  const int32_t* d_rows;    // STORE: nullable [a_rows]: output row of each grouped row (identity if null)
   uint8_t* q_codes;         // SWIGLU: TILED_GROUPED operand with K2 = N/2 (the next GEMM's A)
   const float* gs_q;        // SWIGLU: [G]
   float* h_dump;            // SWIGLU: nullable [a_rows, N/2]
@@ -144,8 +145,8 @@ size_t ep_row_bytes(int H);
 cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s);
 cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes, const int32_t* counts, int G,
                               int El, int shared, int H, uint8_t* a1, int32_t* local_offsets,
-                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* scratch, int* err,
-                              cudaStream_t s);
+                              int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* grp_to_recv,
+                              int32_t* scratch, int* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* in, int64_t n, int64_t row_bytes, const int32_t* idx, void* out,
                                cudaStream_t s);
 

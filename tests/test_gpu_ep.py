@@ -68,7 +68,9 @@ class EmulatedRanks:
             counts.append(cnt[r])
         return torch.cat(rows), torch.stack(counts).contiguous()
 
-    def run(self, w_locals, out_dtype=torch.float32):
+    def run(self, w_locals, out_dtype=torch.float32, fused=False):
+        """fused: the down GEMM stores y rows in received order (row map);
+        else y in grouped order and the return kernel reorders it."""
         nvf, cfg, G = self.nvf, self.cfg, self.G
         y_ret, recv_counts, grouped = [], [], []
         for r in range(G):
@@ -77,8 +79,9 @@ class EmulatedRanks:
             g = nvf.ep_receive(recv, rc, self.El, cfg.shared, cfg.H, n)
             y = nvf.moe_experts(w_locals[r], g["a1"], n, g["offsets"], g["tile_offsets"],
                                 nvf.ep_local_scales(self.gs_a1, cfg.E, G, r, cfg.shared),
-                                nvf.ep_local_scales(self.gs_a2, cfg.E, G, r, cfg.shared), out_dtype)
-            y_ret.append(nvf.ep_return(y, g["recv_to_grp"]))
+                                nvf.ep_local_scales(self.gs_a2, cfg.E, G, r, cfg.shared), out_dtype,
+                                y_rows=g["grp_to_recv"] if fused else None)
+            y_ret.append(y if fused else nvf.ep_return(y, g["recv_to_grp"]))
             recv_counts.append(rc)
             grouped.append(g)
         outs = []
@@ -107,8 +110,11 @@ def test_layer_matches_single_device(nvf, G, shared, Ts):
     tail = [cfg.E] if shared else []
     w_locals = [_weights(nvf, cfg, list(range(r * El, (r + 1) * El)) + tail) for r in range(G)]
     outs, _ = ranks.run(w_locals)
+    fused, _ = ranks.run(w_locals, fused=True)
     code, detail = nvf.device_status()
     assert code == 0, (code, detail)
+    for r in range(G):
+        assert torch.equal(outs[r], fused[r])
     w_full = _weights(nvf, cfg, list(range(cfg.E)) + tail)
     for r in range(G):
         if Ts[r] == 0:
@@ -149,6 +155,7 @@ def test_dispatch_and_receive_match_the_oracle(nvf, shared):
         off, r2g = EP.receive_order(np.stack([plans[s][1][r] for s in range(G)]))
         assert np.array_equal(g["offsets"].cpu().numpy(), off[:El + int(shared) + 1])
         assert np.array_equal(g["recv_to_grp"].cpu().numpy(), r2g)
+        assert np.array_equal(g["grp_to_recv"].cpu().numpy()[r2g], np.arange(n))
         assert np.array_equal(g["tile_offsets"].cpu().numpy(), M.tile_offsets(np.diff(off[:El + int(shared) + 1])))
         # the grouped operand holds each received row at its grouped position
         tile, rr = row_tiles(n, off[:El + int(shared) + 1], g["tile_offsets"].cpu().numpy())
