@@ -402,11 +402,21 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const GemmArgs
             const int na = min(4, k64 - kt * 4);
             const uint32_t st = stage_addr(s);
             const uint32_t sf = tmem + SF_COL0 + s * SF_SLOT_COLS;
-            for (int kk = 0; kk < na; ++kk) {
-              const uint32_t sfa = sf + kk * 4;
-              const uint32_t sfb = sf + 16 + (x.wide ? kk * 8 : kk * 4);
-              tc_mma_nvfp4(tmem, operand_desc_sw128(st + ST_A + kk * 32), operand_desc_sw128(st + ST_B + kk * 32),
-                           idesc, sfa, sfb, (kt | kk) != 0 ? 1u : 0u);
+            // Descriptors once per K tile: K step kk starts 32 bytes further into
+            // the swizzled rows (start address field + 2).  The issuing thread
+            // shares its scheduler with busy epilogue warps, so the fewer
+            // instructions between the MMAs the better.
+            const uint64_t da = operand_desc_sw128(st + ST_A), db = operand_desc_sw128(st + ST_B);
+            const uint32_t sfb_step = x.wide ? 8u : 4u;
+            if (na == 4) {
+              tc_mma_nvfp4(tmem, da, db, idesc, sf, sf + 16, kt != 0 ? 1u : 0u);
+              tc_mma_nvfp4(tmem, da + 2, db + 2, idesc, sf + 4, sf + 16 + sfb_step, 1u);
+              tc_mma_nvfp4(tmem, da + 4, db + 4, idesc, sf + 8, sf + 16 + 2 * sfb_step, 1u);
+              tc_mma_nvfp4(tmem, da + 6, db + 6, idesc, sf + 12, sf + 16 + 3 * sfb_step, 1u);
+            } else {
+              for (int kk = 0; kk < na; ++kk)
+                tc_mma_nvfp4(tmem, da + 2 * kk, db + 2 * kk, idesc, sf + kk * 4, sf + 16 + kk * sfb_step,
+                             (kt | kk) != 0 ? 1u : 0u);
             }
             tc_commit(empty_bar(s));
           }
