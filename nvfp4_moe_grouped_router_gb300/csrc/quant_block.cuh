@@ -69,4 +69,18 @@ __device__ __forceinline__ void store_group64(uint8_t* codes, uint8_t* scales, i
   *reinterpret_cast<uint32_t*>(abase + (gg & 3) * 512 + sf_atom_offset(r, 0)) = sf;
 }
 
+// TILED_GROUPED store of one 64-element group with one 32-byte store for the
+// codes: the group's two 16-byte pieces are the two halves of a 32-byte-aligned
+// block of the swizzled row (swapped when r is odd).  The chunk base must be
+// 32-byte aligned (a 256-byte aligned buffer).
+__device__ __forceinline__ void store_group64_tg32(uint8_t* codes, int K, int64_t tile, uint32_t r, int gg,
+                                                   const uint32_t (&w)[8], uint32_t sf) {
+  uint8_t* cbase = codes + (static_cast<size_t>(tile) * num_k_tiles(K) + (gg >> 2)) * TILE_BYTES;
+  const uint32_t b = static_cast<uint32_t>(gg & 3) * 32u;
+  uint8_t* dst = cbase + r * 128u + ((((b >> 4) ^ (r & 7u)) & ~1u) << 4);
+  if (r & 1u) st_global_v8(dst, w[4], w[5], w[6], w[7], w[0], w[1], w[2], w[3]);
+  else st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+  *reinterpret_cast<uint32_t*>(cbase + TILE_CODE_BYTES + (gg & 3) * 512 + sf_atom_offset(r, 0)) = sf;
+}
+
 }  // namespace nvf

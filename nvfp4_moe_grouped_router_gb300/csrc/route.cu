@@ -45,7 +45,8 @@ namespace {
 
 constexpr int kMaxE = 1024;          // routed experts
 constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
-constexpr int kPermWarps = 16;       // tokens per permute CTA
+constexpr int kPermWarps = 16;       // tokens per permute CTA (up to 256 tokens)
+constexpr int kPermTokWarps = 8;     // tokens per permute CTA (more than 256 tokens: up to 4 CTAs a SM)
 constexpr int kCombineSlots = 8;     // the combine keeps up to this many slots in flight per thread
 
 template <int NV>
@@ -257,8 +258,8 @@ __global__ void __launch_bounds__(kPermWarps * 32) route_small_permute_kernel(Ro
 }
 
 // More than 256 tokens (bitmaps from route_topk_bits_kernel, ranks from
-// route_prefix_kernel; also the empty batch).  Grid (ceil(T / kPermWarps), 1),
-// one warp per token t = bx * kPermWarps + w; lane j places slot j.  With
+// route_prefix_kernel; also the empty batch).  Grid (ceil(T / kPermTokWarps), 1),
+// one warp per token t = bx * kPermTokWarps + w; lane j places slot j.  With
 // PERM_TOKEN the warp then quantizes the row once per distinct global scale
 // among the token's slots and stores it to every slot (the arithmetic is done
 // once per token, not once per slot).
@@ -296,14 +297,14 @@ __device__ __forceinline__ uint32_t quant_packed64(const uint4 (&xr)[8], float g
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kPermWarps * 32, 2) route_permute_kernel(RouteArgs a, int W) {
+__global__ void __launch_bounds__(kPermTokWarps * 32, 4) route_permute_kernel(RouteArgs a, int W) {
   __shared__ int offs[kMaxE + 2];
   __shared__ int til[kMaxE + 2];
-  __shared__ int s_pos[MODE == PERM_TOKEN ? kPermWarps : 1][33];
-  __shared__ int s_exp[MODE == PERM_TOKEN ? kPermWarps : 1][33];
+  __shared__ int s_pos[MODE == PERM_TOKEN ? kPermTokWarps : 1][33];
+  __shared__ int s_exp[MODE == PERM_TOKEN ? kPermTokWarps : 1][33];
   const int E = a.E, Et = a.E + a.shared, k = a.k, T = a.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * kPermWarps + warp;
+  const int t = blockIdx.x * kPermTokWarps + warp;
   // The token's first 64-value group per lane, fetched before the wait on the
   // routing kernels (x does not depend on them).
   uint4 xr[8];
@@ -366,8 +367,8 @@ __global__ void __launch_bounds__(kPermWarps * 32, 2) route_permute_kernel(Route
             gs_done = gs;
           }
           const int local = pj - offs[ej];
-          store_group64(a.a1, nullptr, LAYOUT_TILED_GROUPED, a.H, pj, til[ej] + (local >> 7),
-                        static_cast<uint32_t>(local & 127), gg, w, sf);
+          // one 32-byte store for the codes (the workspace is 256-byte aligned)
+          store_group64_tg32(a.a1, a.H, til[ej] + (local >> 7), static_cast<uint32_t>(local & 127), gg, w, sf);
         }
       }
     }
@@ -527,13 +528,13 @@ cudaError_t launch_route_nv(const RouteArgs& a, cudaStream_t s) {
       if (e != cudaSuccess) return e;
     }
   }
-  const int blocks = a.T > 0 ? (a.T + kPermWarps - 1) / kPermWarps : 1;
+  const int blocks = a.T > 0 ? (a.T + kPermTokWarps - 1) / kPermTokWarps : 1;
   if (a.x != nullptr) {
     prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_TOKEN>));
-    e = launch_kernel(route_permute_kernel<PERM_TOKEN>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
+    e = launch_kernel(route_permute_kernel<PERM_TOKEN>, dim3(blocks), dim3(kPermTokWarps * 32), 0, s, pdl, a, W);
   } else {
     prefer_max_shared(reinterpret_cast<const void*>(route_permute_kernel<PERM_ONLY>));
-    e = launch_kernel(route_permute_kernel<PERM_ONLY>, dim3(blocks), dim3(kPermWarps * 32), 0, s, pdl, a, W);
+    e = launch_kernel(route_permute_kernel<PERM_ONLY>, dim3(blocks), dim3(kPermTokWarps * 32), 0, s, pdl, a, W);
   }
   return e;
 }
