@@ -419,8 +419,8 @@ def _graph_time_us(fn, steps, warmup):
 
 
 def w4a16_sweep(args):
-    """The weight-only path (FP16 activations x NVFP4 weights dequantized in the
-    kernel) beside the W4A4 GEMM on the same weight bytes: (1) the decode layer's
+    """The weight-only path (FP16 or BF16 activations x NVFP4 weights
+    dequantized in the kernel) beside the W4A4 GEMM on the same weight bytes: (1) the decode layer's
     gate_up GEMM (its routing's expert groups, x gathered in permuted order and
     rounded to FP16); (2) the pages' dense gate_up shape N = 34816, K = 5120,
     three weight copies rotating so that weights stream from HBM.  One JSON line
@@ -448,6 +448,14 @@ def w4a16_sweep(args):
                                 f"{touched} experts): us per call", "us_per_call": us,
                       "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm,
                       "algorithmic_bytes": nbytes, "peak_source": src, "steps": steps}), flush=True)
+    # the same call on the BF16 rows as they come (the kernel rounds them to FP16)
+    A_bf = x[r["perm_token"].long()].to(torch.bfloat16).contiguous()
+    us = _graph_time_us(lambda i: nvf.w4a16_grouped_gemm(A_bf, w.w13, w.gs_w13, offs, tiles, 2 * cfg.I, cfg.H, D=D),
+                        steps, args.warmup)
+    print(json.dumps({"metric": "W4A16 grouped GEMM, decode layer gate_up, BF16 activations: us per call",
+                      "us_per_call": us, "gbs": nbytes / (us * 1e-6) / 1e9,
+                      "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm, "algorithmic_bytes": nbytes,
+                      "peak_source": src, "steps": steps}), flush=True)
     del w
     N, K = DENSE_N, DENSE_K
     g = torch.Generator(device="cuda").manual_seed(0)

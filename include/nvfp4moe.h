@@ -93,7 +93,7 @@ typedef enum nvf_status {
   NVF_ERR_DEVICE_CHECK = 6
 } nvf_status;
 
-typedef enum nvf_dtype { NVF_F32 = 0, NVF_BF16 = 1 } nvf_dtype;
+typedef enum nvf_dtype { NVF_F32 = 0, NVF_BF16 = 1, NVF_F16 = 2 } nvf_dtype;
 typedef enum nvf_layout {
   NVF_LAYOUT_ROWMAJOR = 0,
   NVF_LAYOUT_TILED = 1,
@@ -256,20 +256,23 @@ nvf_status nvfp4_grouped_gemm(const uint8_t* A, int64_t a_rows, const uint8_t* B
                               int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream);
 
 /* Weight-only NVFP4 grouped GEMM (W4A16), the decode alternative the pages
- * compare with the W4A4 path: FP16 activations times NVFP4 weights
+ * compare with the W4A4 path: 16-bit activations times NVFP4 weights
  * dequantized in the kernel to FP16 (every e2m1 * e4m3 product is exact in
  * FP16) on the tensor cores (unsloth report, SASS paragraph under "Why it
  * matters": W4A16 unpacks FP4 and runs FP16 MMA; Marlin W4A16 in FlashInfer
  * issue #2723, "Speed Comparison"):
  *   D[row, n] = gs_b[g] * sum_k A[row, k] * dB_g[n, k]   for offsets[g] <= row < offsets[g+1].
- *   A       device fp16 [a_rows, lda], 16-byte aligned, lda >= K and a multiple
- *           of 8 (BF16 activations are converted to FP16, round to nearest, by
- *           the caller).
+ *   A       device [a_rows, lda] of a_dtype, 16-byte aligned, lda >= K and a
+ *           multiple of 8: NVF_F16, or NVF_BF16 (rounded to FP16 by the kernel,
+ *           to nearest: exact for magnitudes in [2^-14, 65504]; larger
+ *           magnitudes become infinities, smaller ones FP16 subnormals).
+ *           Any other a_dtype: NVF_ERR_INVALID_ARG.
  *   B, gs_b, group_offsets, tile_offsets, G, N, K, out_dtype, D, ldd as
  *           nvfp4_grouped_gemm (B the TILED weights of G groups of N rows). */
-nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
-                                    const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G, int32_t N,
-                                    int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream);
+nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int32_t a_dtype, int64_t a_rows, int64_t lda, const uint8_t* B,
+                                    const float* gs_b, const int32_t* group_offsets, const int32_t* tile_offsets,
+                                    int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd,
+                                    void* stream);
 
 /* Prepared expert weights (all device pointers). */
 typedef struct nvf_moe_weights {

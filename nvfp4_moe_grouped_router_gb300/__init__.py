@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
 
-NVF_F32, NVF_BF16 = 0, 1
+NVF_F32, NVF_BF16, NVF_F16 = 0, 1, 2
 LAYOUT_ROWMAJOR, LAYOUT_TILED, LAYOUT_TILED_GROUPED = 0, 1, 2
 TILE_BYTES = 18432   # one (128-row, 256-K) chunk: 16 KB swizzled codes + 2 KB scale atoms
 STATUS = {0: "NVF_OK", 1: "NVF_ERR_INVALID_ARG", 2: "NVF_ERR_UNSUPPORTED_DEVICE", 3: "NVF_ERR_WORKSPACE",
@@ -45,8 +45,8 @@ SIGNATURES = {
     "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
                                          _P]),
     "nvf_router_gemm": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P]),
-    "nvfp4_w4a16_grouped_gemm": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64,
-                                                _P]),
+    "nvfp4_w4a16_grouped_gemm": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P,
+                                                _I64, _P]),
     "nvfp4_moe_forward_gated": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ,
                                                _P]),
     "nvf_ep_row_bytes": (_SZ, [_I32]),
@@ -220,17 +220,19 @@ def grouped_gemm(A, a_rows: int, B, gs_a, gs_b, offsets, tile_offsets, N: int, K
 
 
 def w4a16_grouped_gemm(A, B, gs_b, offsets, tile_offsets, N: int, K: int, out_dtype=torch.float32, D=None):
-    """D[row] = gs_b[g] A[row] . dB[g]^T for the rows of group g: A fp16 [rows, K]
-    (row-major, grouped by offsets), B the TILED weights of the groups."""
+    """D[row] = gs_b[g] A[row] . dB[g]^T for the rows of group g: A fp16 or bf16
+    [rows, K] (row-major, grouped by offsets; bf16 is rounded to fp16 by the
+    kernel), B the TILED weights of the groups."""
     _cuda(A, "A")
-    if A.dtype != torch.float16:
-        raise TypeError("A must be float16")
+    if A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A must be float16 or bfloat16")
     G = offsets.numel() - 1
     rows = A.shape[0]
     if D is None:
         D = torch.zeros(max(rows, 1), N, dtype=out_dtype, device=A.device)
     code = NVF_F32 if D.dtype == torch.float32 else NVF_BF16
-    _check(lib().nvfp4_w4a16_grouped_gemm(_ptr(A), rows, A.stride(0), _ptr(B), _ptr(gs_b), _ptr(offsets),
+    a_code = NVF_F16 if A.dtype == torch.float16 else NVF_BF16
+    _check(lib().nvfp4_w4a16_grouped_gemm(_ptr(A), a_code, rows, A.stride(0), _ptr(B), _ptr(gs_b), _ptr(offsets),
                                           _ptr(tile_offsets), G, N, K, code, _ptr(D), D.stride(0), _stream()))
     return D
 

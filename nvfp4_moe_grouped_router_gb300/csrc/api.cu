@@ -565,22 +565,25 @@ nvf_status nvfp4_moe_forward_gated(const nvf_moe_weights* w, const void* w_gate,
                       nullptr, ws, ws_bytes, nullptr, stream);
 }
 
-nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
-                                    const int32_t* group_offsets, const int32_t* tile_offsets, int32_t G, int32_t N,
-                                    int32_t K, int32_t out_dtype, void* D, int64_t ldd, void* stream) {
+nvf_status nvfp4_w4a16_grouped_gemm(const void* A, int32_t a_dtype, int64_t a_rows, int64_t lda, const uint8_t* B,
+                                    const float* gs_b, const int32_t* group_offsets, const int32_t* tile_offsets,
+                                    int32_t G, int32_t N, int32_t K, int32_t out_dtype, void* D, int64_t ldd,
+                                    void* stream) {
   NVF_BEGIN();
   {
     nvf_status s = validate_gemm(static_cast<const uint8_t*>(A), a_rows, B, G, N, K);
     if (s != NVF_OK) return s;
   }
   NVF_REQUIRE(gs_b && group_offsets && tile_offsets && D, "gs_b, offsets and D must not be NULL");
+  NVF_REQUIRE(a_dtype == NVF_F16 || a_dtype == NVF_BF16, "a_dtype=%d must be NVF_F16 or NVF_BF16", a_dtype);
   NVF_REQUIRE(lda >= K && lda % 8 == 0, "lda=%lld must be >= K=%d and a multiple of 8", (long long)lda, K);
   NVF_REQUIRE(out_dtype == NVF_F32 || out_dtype == NVF_BF16, "out_dtype=%d must be NVF_F32 or NVF_BF16", out_dtype);
   const int esz = out_dtype == NVF_F32 ? 4 : 2;
   NVF_REQUIRE(ldd >= N && (ldd * esz) % 16 == 0 && aligned16(D),
               "D must be 16-byte aligned with ldd >= N=%d and ldd*%d bytes a multiple of 16 (ldd=%lld)", N, esz,
               (long long)ldd);
-  NVF_CUDA(launch_w4a16(A, a_rows, lda, B, gs_b, group_offsets, tile_offsets, G, N, K, out_dtype == NVF_BF16, D, ldd,
+  NVF_CUDA(launch_w4a16(A, a_dtype == NVF_BF16, a_rows, lda, B, gs_b, group_offsets, tile_offsets, G, N, K,
+                        out_dtype == NVF_BF16, D, ldd,
                         dev_->err, static_cast<cudaStream_t>(stream)),
            "W4A16 GEMM launch");
   return NVF_OK;

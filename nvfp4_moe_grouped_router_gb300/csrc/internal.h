@@ -86,9 +86,9 @@ cudaError_t launch_combine(const void* y, int32_t H, const float* weights, const
                            int32_t k, int32_t shared, int dtype, void* out, cudaStream_t s, bool pdl,
                            const float* shared_gate = nullptr, int64_t ldg = 0);
 
-// Weight-only NVFP4 grouped GEMM: FP16 A [a_rows, lda] rows grouped by offsets, B the
+// Weight-only NVFP4 grouped GEMM: FP16 (or BF16, a_bf16) A [a_rows, lda] rows grouped by offsets, B the
 // TILED weights of G groups of N rows, D [rows, ldd] FP32 (out_bf16 = 0) or BF16.
-cudaError_t launch_w4a16(const void* A, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
+cudaError_t launch_w4a16(const void* A, int a_bf16, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
                          const int32_t* offsets, const int32_t* tile_offs, int32_t G, int32_t N, int32_t K,
                          int out_bf16, void* D, int64_t ldd, int* err, cudaStream_t s);
 

@@ -1,6 +1,6 @@
 // Weight-only NVFP4 grouped GEMM (W4A16) for sm_103a:
 //     D[row, n] = gs_b[g] * sum_k a[row, k] * dB_g[n, k]   for offsets[g] <= row < offsets[g+1]
-// with FP16 activations a and NVFP4 weights dB = e2m1 * e4m3 dequantized in the
+// with FP16 activations a (BF16 ones are rounded to FP16 in the kernel) and NVFP4 weights dB = e2m1 * e4m3 dequantized in the
 // kernel and multiplied on the tensor cores as FP16 (tcgen05.mma kind::f16).
 // This is the decode alternative the pages keep comparing with the W4A4 path:
 // W4A16 unpacks FP4 weights and runs FP16 MMA (unsloth report, SASS paragraph
@@ -23,6 +23,9 @@
 //   ACT_WARP     copies the token tile's activations (cp.async, 16 bytes a lane)
 //                into 128-byte-swizzled K-major rows, one 64-element K step a
 //                16 KB stage (4 stages), completing each stage's mbarrier;
+//   CVT_WARP     BF16 activations only: waits for each landed stage, rounds it
+//                to FP16 in place and completes the stage for the MMA (so the
+//                copies stay as deep in flight as for FP16 rows);
 //   warps 0-15   convert: warpgroup (par, j) owns weight tile j of the pair for
 //                the K steps of parity par, thread (quarter q, lane l) its row
 //                32 q + l: per K step it reads the row's 32 code bytes and 4
@@ -55,7 +58,8 @@ namespace {
 
 constexpr int DQ_WARPS = 16;
 constexpr int MMA_WARP0 = 16, N_MMA = 2, EPI_WARP0 = MMA_WARP0 + N_MMA, RAW_WARP = EPI_WARP0 + 4, ACT_WARP = RAW_WARP + 1;
-constexpr int W_THREADS = 32 * (ACT_WARP + 1);
+constexpr int CVT_WARP = ACT_WARP + 1;            // BF16 activations: rounds each landed stage to FP16
+constexpr int W_THREADS = 32 * (CVT_WARP + 1);
 constexpr int RAW_STAGES = 4;
 constexpr int RAW_STAGE = 2 * TILE_BYTES;        // 36864: one K tile of a weight pair
 constexpr int SLOTS = 4;                         // activation stages = TMEM weight slots
@@ -64,8 +68,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int A_COL = 256;
 constexpr int OFF_ACT = RAW_STAGES * RAW_STAGE;  // 147456
 constexpr int OFF_BAR = OFF_ACT + SLOTS * ACT_STAGE;
-// raw_full[4] raw_empty[4] act_full[4] a_full[4] mma_done[4] d_full d_empty drain[N_MMA]
-constexpr int NUM_BARS = 2 * RAW_STAGES + 3 * SLOTS + 2 + N_MMA;
+// raw_full[4] raw_empty[4] act_full[4] a_full[4] mma_done[4] d_full d_empty drain[N_MMA] act_landed[4]
+constexpr int NUM_BARS = 2 * RAW_STAGES + 4 * SLOTS + 2 + N_MMA;
 constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr int W_SMEM = OFF_MISC + 16 + 1024;     // + alignment slack
 
@@ -103,7 +107,8 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 struct W16Args {
-  const __half* a;
+  const __half* a;          // FP16 rows, or BF16 rows when a_bf16 (16-bit elements either way)
+  int a_bf16;
   int64_t a_rows, lda;
   const uint8_t* b;
   const float* gs_b;
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) w4a16_kernel(const W16Args a) {
   auto a_full = [&](int s) { return bar0 + 8u * (2 * RAW_STAGES + SLOTS + s); };
   auto mma_done = [&](int s) { return bar0 + 8u * (2 * RAW_STAGES + 2 * SLOTS + s); };
   const uint32_t d_full = bar0 + 8u * (2 * RAW_STAGES + 3 * SLOTS), d_empty = d_full + 8, drain_bar0 = d_full + 16;
+  auto act_landed = [&](int s) { return drain_bar0 + 8u * (N_MMA + s); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -156,6 +162,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) w4a16_kernel(const W16Args a) {
       mbar_init(act_full(s), 32);
       mbar_init(a_full(s), DQ_WARPS / 2);                 // the 8 warps of the step's parity
       mbar_init(mma_done(s), N_MMA);
+      mbar_init(act_landed(s), 32);
     }
     mbar_init(d_full, N_MMA);
     mbar_init(d_empty, 4);
@@ -221,10 +228,51 @@ __global__ void __launch_bounds__(W_THREADS, 1) w4a16_kernel(const W16Args a) {
           const int r = q >> 3, c = q & 7;
           cp_async16(st + r * 128 + ((c ^ (r & 7)) << 4), arow + static_cast<int64_t>(r) * a.lda + ks * 64 + c * 8);
         }
-        cp_async_mbar_arrive(act_full(s));
+        // FP16 rows are the MMA's operand as they land; BF16 rows go to the
+        // rounding warp first
+        cp_async_mbar_arrive(a.a_bf16 ? act_landed(s) : act_full(s));
       }
     }
     cp_async_wait_all();
+  } else if (warp == CVT_WARP) {
+    // ------------------------------------------------------------------ BF16 -> FP16
+    // Each lane rounds the 16-byte chunks of a landed stage (BF16 pairs -> FP16
+    // pairs, to nearest) in place; then the stage is the MMA's operand.
+    if (a.a_bf16) {
+      uint32_t sc = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        const Item x = decode_item(it, n_pairs, ntg, a);
+        for (int ks = 0; ks < nks; ++ks, ++sc) {
+          const int s = sc % SLOTS;
+          const bool got = mbar_wait(act_landed(s), (sc / SLOTS) & 1u, abort_flag, a.err, DEV_TIMEOUT_PRODUCER, it);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = s_base + OFF_ACT + s * ACT_STAGE;
+          for (int q = lane; q < x.rows * 8; q += 32) {
+            const int r = q >> 3, c = q & 7;
+            const uint32_t addr = st + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t w[4];
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "r"(addr)
+                         : "memory");
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half2 v = __floats2half2_rn(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+              w[e] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+          }
+          fence_proxy_async();                  // the MMA reads the stage through the async proxy
+          mbar_arrive(act_full(s));
+        }
+      }
+    }
   } else if (warp >= MMA_WARP0 && warp < EPI_WARP0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ MMA issuers
@@ -373,7 +421,7 @@ __global__ void __launch_bounds__(W_THREADS, 1) w4a16_kernel(const W16Args a) {
 
 }  // namespace
 
-cudaError_t launch_w4a16(const void* A, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
+cudaError_t launch_w4a16(const void* A, int a_bf16, int64_t a_rows, int64_t lda, const uint8_t* B, const float* gs_b,
                          const int32_t* offsets, const int32_t* tile_offs, int32_t G, int32_t N, int32_t K,
                          int out_bf16, void* D, int64_t ldd, int* err, cudaStream_t s) {
   if (a_rows <= 0) return cudaSuccess;
@@ -383,8 +431,8 @@ cudaError_t launch_w4a16(const void* A, int64_t a_rows, int64_t lda, const uint8
   const int64_t n_pairs = (N / TILE_ROWS + 1) / 2;
   const int64_t max_items = ((a_rows + TILE_ROWS - 1) / TILE_ROWS + G) * n_pairs;
   const int grid = static_cast<int>(max_items < sm_count() ? max_items : sm_count());
-  W16Args args{static_cast<const __half*>(A), a_rows, lda, B, gs_b, offsets, tile_offs, G, N, K, out_bf16, D, ldd,
-               err};
+  W16Args args{static_cast<const __half*>(A), a_bf16, a_rows, lda, B, gs_b, offsets, tile_offs, G, N, K, out_bf16, D,
+               ldd, err};
   w4a16_kernel<<<grid, W_THREADS, W_SMEM, s>>>(args);
   return cudaGetLastError();
 }

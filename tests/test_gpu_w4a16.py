@@ -1,7 +1,7 @@
 """GPU parity of the weight-only NVFP4 grouped GEMM (W4A16) against the oracle.
 
-Activations are FP16 values (BF16 inputs rounded to FP16 by the caller, the
-same values on both sides).  An exact special case (power-of-two scales,
+Activations are FP16 values, or BF16 values that the kernel rounds to FP16
+(the oracle takes the same rounded values).  An exact special case (power-of-two scales,
 small-integer activations, codes from the E2M1 table) must match bit for bit
 and pins the nibble order and the scale placement; random cases must stay
 within 5e-3 * rms of the oracle's float64 result.
@@ -28,7 +28,7 @@ def _pack(q):
     return (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
 
 
-def _run(nvf, a_f16, sizes, w_codes, w_scales, gs_w, out_dtype=torch.float32):
+def _run(nvf, a_f16, sizes, w_codes, w_scales, gs_w, out_dtype=torch.float32, a_torch=None):
     sizes = np.asarray(sizes, np.int64)
     G, N, Kh = w_codes.shape
     K = 2 * Kh
@@ -36,9 +36,9 @@ def _run(nvf, a_f16, sizes, w_codes, w_scales, gs_w, out_dtype=torch.float32):
     tiles = M.tile_offsets(sizes)
     B = weight_pack(w_codes.reshape(G * N, Kh), w_scales.reshape(G * N, K // 16), K, N, nvf.tiled_bytes(G * N, 0, K))
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    A = torch.from_numpy(np.ascontiguousarray(a_f16)).cuda()
+    A = a_torch.cuda() if a_torch is not None else torch.from_numpy(np.ascontiguousarray(a_f16)).cuda()
     if A.shape[0] == 0:
-        A = torch.zeros(1, K, dtype=torch.float16, device="cuda")
+        A = torch.zeros(1, K, dtype=A.dtype, device="cuda")
     D = nvf.w4a16_grouped_gemm(A[: max(int(offs[-1]), 1)], dev(B), dev(np.asarray(gs_w, np.float32)),
                                dev(offs.astype(np.int32)), dev(tiles.astype(np.int32)), N, K, out_dtype)
     code, detail = nvf.device_status()
@@ -114,6 +114,42 @@ def test_many_items_per_cta(nvf, N, K):
     assert rel_err(D, M.grouped_w4a16(a.astype(np.float64), offs, w_c, w_s, gs_w)) <= TOL
 
 
+def test_bf16_activations_exact(nvf):
+    """Small integers are exact in BF16 and FP16: BF16 input gives the oracle's bits."""
+    rng = np.random.default_rng(7)
+    sizes = [40, 1, 129]
+    G, N, K = len(sizes), 256, 256
+    R = sum(sizes)
+    q_w = rng.integers(0, 16, (G, N, K)).astype(np.uint8)
+    s_w = np.array([0x30, 0x38, 0x40], np.uint8)[rng.integers(0, 3, (G, N, K // 16))]
+    a = rng.integers(-4, 5, (R, K)).astype(np.float32)
+    gs = np.ones(G, np.float32)
+    D, offs = _run(nvf, None, sizes, _pack(q_w), s_w, gs, a_torch=torch.from_numpy(a).to(torch.bfloat16))
+    ref = M.grouped_w4a16(a.astype(np.float64), offs, _pack(q_w), s_w, gs)
+    assert np.array_equal(D, ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_bf16_activations_random(nvf, out_dtype):
+    """BF16 activations are rounded to FP16 by the kernel: the result equals the
+    FP16 path on the rounded values bit for bit, and the oracle on them within
+    the tolerance."""
+    rng = np.random.default_rng(8)
+    sizes = [0, 3, 130, 17]
+    G, N, K = len(sizes), 384, 320
+    R = sum(sizes)
+    a_bf = torch.randn(R, K, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    a16 = a_bf.to(torch.float16).numpy()           # round to nearest, what the kernel does
+    w_c, w_s, gs_w = _random_weights(rng, G, N, K)
+    D_bf, offs = _run(nvf, None, sizes, w_c, w_s, gs_w, out_dtype, a_torch=a_bf)
+    D_16, _ = _run(nvf, a16, sizes, w_c, w_s, gs_w, out_dtype)
+    assert np.array_equal(D_bf, D_16)
+    ref = M.grouped_w4a16(a16.astype(np.float64), offs, w_c, w_s, gs_w)
+    rms = np.sqrt(np.mean(ref ** 2))
+    bound = TOL * rms + (np.abs(ref) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0)
+    assert np.all(np.abs(D_bf - ref) <= bound)
+
+
 def test_argument_validation(nvf):
     z = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     a = torch.zeros(4, 100, dtype=torch.float16, device="cuda")
@@ -123,3 +159,9 @@ def test_argument_validation(nvf):
         nvf.w4a16_grouped_gemm(a, z, f, o, o, 128, 100)
     with pytest.raises(TypeError):
         nvf.w4a16_grouped_gemm(a.float(), z, f, o, o, 128, 64)
+    # an activation type code other than FP16 / BF16, straight through the C ABI
+    D = torch.zeros(4, 128, device="cuda")
+    st = nvf.lib().nvfp4_w4a16_grouped_gemm(a.data_ptr(), nvf.NVF_F32, 4, 100, z.data_ptr(), f.data_ptr(),
+                                            o.data_ptr(), o.data_ptr(), 1, 128, 64, nvf.NVF_F32, D.data_ptr(), 128,
+                                            None)
+    assert st == 1 and b"a_dtype" in nvf.lib().nvf_last_error_message()
