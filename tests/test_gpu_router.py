@@ -68,11 +68,12 @@ def _layer(cfg):
     return x
 
 
-@pytest.mark.parametrize("gated", [False, True])
-def test_layer_from_hidden_states(nvf, gated):
+@pytest.mark.parametrize("gated,T", [(False, 40), (True, 40), (True, 300)])
+def test_layer_from_hidden_states(nvf, gated, T):
     """Router gate + layer, with and without the shared expert's gate, against
-    the oracle on the GPU's logits; routing bit-exact."""
-    cfg = CONFIGS["tiny"].scaled(T=40, shared=True, name="tiny_shared")
+    the oracle on the GPU's logits; routing bit-exact.  40 tokens take the
+    CUDA-core gate, 300 the tensor-core one (K split over a cluster)."""
+    cfg = CONFIGS["tiny"].scaled(T=T, shared=True, name="tiny_shared")
     x = _layer(cfg)
     wg = gate_weights(cfg, 0, shared_gate=gated)
     w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, True, lambda e: expert_weights(cfg, e, 0))
