@@ -820,16 +820,25 @@ def prefill_object(nvf, w, seed, K, warmup, hbm, fp4_peak, src):
     return obj
 
 
+def gemm_sources_sha():
+    """sha256 (16 hex digits) of the GEMM kernel's sources: gemm.cu and the
+    headers it includes, concatenated in this order."""
+    from nvfp4_moe_grouped_router_gb300 import build as b
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "quant_block.cuh", "layout.cuh", "ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(b.CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profiles(name):
     p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    from nvfp4_moe_grouped_router_gb300 import build as b
-    import hashlib
-    h = hashlib.sha256(open(os.path.join(b.CSRC, "gemm.cu"), "rb").read()).hexdigest()[:16]
+    h = gemm_sources_sha()
     e = d.get(name)
-    if not e or e.get("gemm_cu_sha") != h:
+    if not e or e.get("gemm_sources_sha") != h:
         return None
     return e.get("bytes_per_launch")
 

@@ -2,9 +2,9 @@
 // fused route+quantize kernel and the GEMM1 epilogue (which requantizes
 // h = silu(gate) * up): FP32 amax, E4M3 block scale of amax / (6 gs),
 // reciprocal of dec(scale) * gs, E2M1 codes of x * r.  Every step is a single
-// correctly rounded FP32 operation or a round-to-nearest-even satfinite
-// conversion instruction.  Also the stores of 64-element groups into each
-// operand layout.
+// correctly rounded FP32 operation (the products two per f32x2 multiply) or a
+// round-to-nearest-even satfinite conversion instruction.  Also the stores of
+// 64-element groups into each operand layout.
 #pragma once
 #include "layout.cuh"
 #include "ptx.cuh"
@@ -21,11 +21,8 @@ __device__ __forceinline__ uint32_t quant_block16(const float* v, float gs, floa
   const uint32_t sb = cvt_e4m3(__fdiv_rn(amax, six_gs));
   const float t3 = __fmul_rn(e4m3_to_f32(sb), gs);
   const float r = (t3 == 0.0f) ? 0.0f : __frcp_rn(t3);
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = cvt_e2m1x2(__fmul_rn(v[2 * j], r), __fmul_rn(v[2 * j + 1], r));
-  w0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  w1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  w0 = e2m1x8_scaled(v, r);
+  w1 = e2m1x8_scaled(v + 8, r);
   return sb;
 }
 
