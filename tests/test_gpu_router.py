@@ -37,8 +37,14 @@ def _check_logits(got, xb, wb):
     return ref
 
 
+# Above 64 tokens the K split is the largest power of two S <= 8 with
+# ceil(T / 128) * ceil(n / 256) * S <= SMs (152) that divides H / 64: 65 and
+# 128 tokens run S = 4 (H = 256), 300 tokens S = 8, 4096 tokens S = 4, 6000
+# tokens S = 2, 10000 tokens S = 1 (a cluster of one); 513 gate rows take
+# three 256-row blocks, the last with 16.
 @pytest.mark.parametrize("T,H,n", [(1, 256, 8), (37, 2048, 129), (64, 128, 9), (65, 256, 33), (128, 256, 33),
-                                   (300, 2048, 128), (4096, 2048, 129), (256, 4096, 513)])
+                                   (300, 2048, 128), (4096, 2048, 129), (256, 4096, 513), (6000, 512, 40),
+                                   (10000, 256, 33)])
 def test_router_gemm_matches_the_oracle(nvf, T, H, n):
     g = torch.Generator().manual_seed(T + H + n)
     x = torch.randn(T, H, generator=g).to(torch.bfloat16)
