@@ -620,6 +620,7 @@ def main():
     t = run.time(K, args.warmup, dist, rank, e2e=True)
     elapsed_ms, value = job_time_and_value(t["elapsed_ms"], cfg.T, K, dist, "cuda")
     _, e2e_value = job_time_and_value(t["e2e_ms"], cfg.T, t["e2e_steps"], dist, "cuda")
+    _, e2e_calls_value = job_time_and_value(t["e2e_eager_ms"], cfg.T, t["e2e_steps"], dist, "cuda")
     touched, lbytes = layer_bytes(cfg, t["counts"])
     ms_step = elapsed_ms / K
     gemms = gemm_rooflines(cfg, t, touched, hbm, fp4_peak, src)
@@ -640,7 +641,9 @@ def main():
             "layer_hbm_frac": lbytes / (ms_step * 1e-3) / 1e9 / hbm, "touched_experts": touched,
             "gemms": gemms, "roofline": roof, "clocks": t["clocks"], "gpu_launches": kernels_per_step(cfg.T) * K,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": t["h2d"],
-                    "d2h_bytes_per_step": t["d2h"]}}
+                    "d2h_bytes_per_step": t["d2h"],
+                    "path": "nvf_moe_graph_launch: copies in, the layer, copy out as one CUDA graph a step",
+                    "separate_calls_value": e2e_calls_value}}
     del run
     if cfg.name == "decode" and world == 1:
         line["prefill"] = prefill_object(nvf, w, seed + rank, min(K, 100), args.warmup, hbm, fp4_peak, src)
@@ -748,14 +751,34 @@ class LayerRun:
         res["stage_step_ms"] = statistics.mean(ev[i][0].elapsed_time(ev[i][5]) for i in range(chunk))
         res["counts"] = self.counts()
         if e2e:
-            # end to end through the C ABI with host buffers: H2D of x and logits
-            # from pinned memory, the layer, D2H of out, every step
+            # End to end through the C ABI with host buffers: every step copies x
+            # and logits in from page-locked host memory, runs the layer and
+            # copies out back.  Served as a decode engine would: the step is one
+            # CUDA graph (nvf_moe_graph_create / _launch); the same step as
+            # separate calls from Python (copies, nvfp4_moe_forward, copy) is
+            # reported beside it.
+            c = self.cfg
+            g = self.nvf.MoEGraph(self.w, c.T, c.k, self.gs_a1, self.gs_a2, bias=self.bias,
+                                  renormalize=c.renormalize, out_dtype=self.out.dtype)
+            g.x.copy_(self.x.cpu())
+            g.logits.copy_(self.logits.cpu())
+            Ke = min(K, 200)
+            for _ in range(3):
+                g.launch()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(Ke):
+                g.launch()
+            e1.record()
+            torch.cuda.synchronize()
+            self.check()
+            graph_ms = e0.elapsed_time(e1)
+            g.close()
             xh, lh = self.x.cpu().pin_memory(), self.logits.cpu().pin_memory()
             oh = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
             xd, ld = torch.empty_like(self.x), torch.empty_like(self.logits)
-            Ke = min(K, 200)
             torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             for _ in range(Ke):
                 xd.copy_(xh, non_blocking=True)
@@ -765,8 +788,8 @@ class LayerRun:
             e1.record()
             torch.cuda.synchronize()
             self.check()
-            res.update(e2e_ms=e0.elapsed_time(e1), e2e_steps=Ke, h2d=self.x.numel() * 2 + self.logits.numel() * 4,
-                       d2h=self.out.numel() * 2)
+            res.update(e2e_ms=graph_ms, e2e_eager_ms=e0.elapsed_time(e1), e2e_steps=Ke,
+                       h2d=self.x.numel() * 2 + self.logits.numel() * 4, d2h=self.out.numel() * self.out.element_size())
         return res
 
 

@@ -325,6 +325,38 @@ nvf_status nvfp4_moe_forward(const nvf_moe_weights* w, const void* x, const floa
                              int32_t out_dtype, void* out, float* h_dump, void* ws, size_t ws_bytes,
                              void* const* stage_events, void* stream);
 
+/* A step of the layer captured once as a CUDA graph, for serving a fixed
+ * batch: the host-to-device copies of x and logits from caller-owned
+ * page-locked host buffers, nvfp4_moe_forward, and the device-to-host copy of
+ * out, replayed by one call.  The copies are kernels that move the bytes
+ * through the device's mapping of the page-locked buffers.  It removes the per-step launch work of the
+ * separate calls (a decode step's kernels take tens of microseconds; their
+ * launches from a host language take as long).
+ *   w, gs_a1, gs_a2, bias (NULL or device float[E]): as nvfp4_moe_forward;
+ *             the device buffers they point to must outlive the graph.
+ *   x_host    page-locked host bf16 [T, H]; logits_host page-locked host
+ *             float [T, E]; out_host page-locked host [T, H] of out_dtype
+ *             (NVF_F32 or NVF_BF16); all 16-byte aligned.  Each launch reads x_host and
+ *             logits_host and writes out_host, asynchronously on the launch
+ *             stream: fill the inputs before the launch, read out_host after
+ *             the stream has reached the launch.  Pageable host memory:
+ *             NVF_ERR_INVALID_ARG.  When logits_host starts right where
+ *             x_host ends (T * H * 2 bytes on), both travel in one copy.
+ *   graph     receives the handle.  The graph owns its device copies of x,
+ *             logits and out and the forward's workspace (freed by
+ *             nvf_moe_graph_destroy).
+ * Capture does not run the step.  Errors of a launched step are reported
+ * through nvf_device_status like those of the separate calls. */
+typedef struct nvf_moe_graph nvf_moe_graph;
+nvf_status nvf_moe_graph_create(const nvf_moe_weights* w, int32_t T, int32_t k, int32_t renormalize,
+                                const float* gs_a1, const float* gs_a2, const float* bias, const void* x_host,
+                                const float* logits_host, void* out_host, int32_t out_dtype, nvf_moe_graph** graph);
+/* Launch the captured step on `stream` (asynchronous). */
+nvf_status nvf_moe_graph_launch(nvf_moe_graph* graph, void* stream);
+/* Free the graph and its device buffers (after its launches have completed).
+ * NULL is a no-op. */
+nvf_status nvf_moe_graph_destroy(nvf_moe_graph* graph);
+
 /* Router gate, the step before routing: logits[t * ldl + j] = sum_h x[t, h] *
  * w_gate[j, h] for j < n, with BF16 inputs multiplied on the tensor cores and
  * summed in FP32.

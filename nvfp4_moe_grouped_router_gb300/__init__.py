@@ -45,6 +45,10 @@ SIGNATURES = {
     "nvfp4_moe_forward": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P,
                                          _P]),
     "nvf_router_gemm": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _I64, _P]),
+    "nvf_moe_graph_create": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _I32,
+                                            ctypes.POINTER(ctypes.c_void_p)]),
+    "nvf_moe_graph_launch": (ctypes.c_int, [_P, _P]),
+    "nvf_moe_graph_destroy": (ctypes.c_int, [_P]),
     "nvfp4_w4a16_grouped_gemm": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P,
                                                 _I64, _P]),
     "nvfp4_moe_forward_gated": (ctypes.c_int, [_P, _P, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _SZ,
@@ -312,6 +316,45 @@ def moe_forward(w: MoEWeights, x, logits, k: int, gs_a1, gs_a2, bias=None, renor
                                    _ptr(gs_a1), _ptr(gs_a2), NVF_F32 if out.dtype == torch.float32 else NVF_BF16,
                                    _ptr(out), _ptr(h_dump), _ptr(ws), ws.numel(), ev, _stream()))
     return out
+
+
+class MoEGraph:
+    """One step of the layer captured as a CUDA graph (nvf_moe_graph_create):
+    host-to-device copies of `x` and `logits` from page-locked host tensors,
+    the layer, and the copy of the result into the page-locked host tensor
+    `out`, all replayed by launch().  Fill x / logits, launch(), and read out
+    after synchronizing the stream."""
+
+    def __init__(self, w: MoEWeights, T: int, k: int, gs_a1, gs_a2, bias=None, renormalize=True,
+                 out_dtype=torch.bfloat16):
+        # x and logits in one page-locked buffer, logits right behind x: one copy a step
+        xb, lb = T * w.H * 2, T * w.E * 4
+        self._inputs = torch.zeros(xb + lb, dtype=torch.uint8).pin_memory()
+        self.x = self._inputs[:xb].view(torch.bfloat16).view(T, w.H)
+        self.logits = self._inputs[xb:].view(torch.float32).view(T, w.E)
+        self.out = torch.zeros(T, w.H, dtype=out_dtype).pin_memory()
+        self._keep = (w, gs_a1, gs_a2, bias)        # device buffers the graph reads
+        cw = w.c_struct()
+        h = ctypes.c_void_p()
+        _check(lib().nvf_moe_graph_create(ctypes.byref(cw), T, k, int(renormalize), _ptr(gs_a1), _ptr(gs_a2),
+                                          _ptr(bias), _ptr(self.x), _ptr(self.logits), _ptr(self.out),
+                                          NVF_F32 if out_dtype == torch.float32 else NVF_BF16, ctypes.byref(h)))
+        self._h = h
+
+    def launch(self):
+        _check(lib().nvf_moe_graph_launch(self._h, _stream()))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            torch.cuda.synchronize()
+            lib().nvf_moe_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def router_gemm(x, w_gate, logits=None):
