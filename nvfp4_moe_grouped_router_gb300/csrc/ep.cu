@@ -95,6 +95,93 @@ __global__ void __launch_bounds__(128) ep_dispatch_kernel(EpDispatchArgs a) {
   }
 }
 
+// Above 256 tokens the dispatch runs token by token, so that a token is
+// quantized once per distinct global scale among its slots (once, when every
+// expert shares one) instead of once per slot.  Pass 1, one thread per
+// permuted row: the row's send position into src_to_send, and its expert id
+// into the first 4 bytes of its send row, where pass 2 reads it before it
+// writes the row.
+__global__ void __launch_bounds__(256) ep_dispatch_place_kernel(EpDispatchArgs a) {
+  __shared__ int64_t send_off[kEpMaxRanks + 1];
+  const int El = a.E / a.G, Et = a.E + a.shared;
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    for (int r = 0; r < a.G; ++r) {
+      send_off[r] = acc;
+      acc += __ldg(a.offsets + (r + 1) * El) - __ldg(a.offsets + r * El);
+      if (r == a.rank && a.shared) acc += __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+    }
+    send_off[a.G] = acc;
+  }
+  if (blockIdx.x == 0) {
+    for (int c = threadIdx.x; c < a.G * (El + 1); c += blockDim.x) {
+      const int r = c / (El + 1), j = c - r * (El + 1);
+      int n = 0;
+      if (j < El) n = __ldg(a.offsets + r * El + j + 1) - __ldg(a.offsets + r * El + j);
+      else if (r == a.rank && a.shared) n = __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+      a.send_counts[c] = n;
+    }
+  }
+  __syncthreads();
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t R = __ldg(a.offsets + Et);
+  if (p >= R) return;
+  const int e = upper_group(a.offsets, Et, p);
+  int64_t pos;
+  if (e < a.E) {
+    const int dest = e / El;
+    pos = send_off[dest] + (p - __ldg(a.offsets + dest * El));
+  } else {
+    const int64_t own_routed = __ldg(a.offsets + (a.rank + 1) * El) - __ldg(a.offsets + a.rank * El);
+    pos = send_off[a.rank] + own_routed + (p - __ldg(a.offsets + a.E));
+  }
+  a.src_to_send[__ldg(a.perm_to_src + p)] = static_cast<int32_t>(pos);
+  *reinterpret_cast<int32_t*>(a.send + pos * static_cast<int64_t>(a.row_bytes)) = e;
+}
+
+// Pass 2, one warp per token: lane j first reads slot j's send position and
+// expert (every slot's before any lane writes a row), then each lane quantizes
+// its 16-element blocks of the token once per distinct global scale and writes
+// them to every slot's row.
+constexpr int kDispatchTokWarps = 8;
+__global__ void __launch_bounds__(kDispatchTokWarps * 32) ep_dispatch_token_kernel(EpDispatchArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kDispatchTokWarps + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const int slots = a.k + a.shared;
+  int pos_j = 0, e_j = 0;
+  if (lane < slots) {
+    const int64_t as = lane < a.k ? static_cast<int64_t>(t) * a.k + lane : static_cast<int64_t>(a.T) * a.k + t;
+    pos_j = __ldg(a.src_to_send + as);
+    e_j = *reinterpret_cast<const int32_t*>(a.send + static_cast<int64_t>(pos_j) * a.row_bytes);
+  }
+  __syncwarp();
+  const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) + static_cast<int64_t>(t) * a.H);
+  for (int b = lane; b < a.H / 16; b += 32) {
+    const uint4 u0 = __ldg(xr + 2 * b), u1 = __ldg(xr + 2 * b + 1);
+    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(wv[i] << 16);               // bf16 -> fp32 is exact
+      v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+    }
+    float gs_done = -1.0f;                                   // global scales are positive
+    uint32_t w0 = 0, w1 = 0, sb = 0;
+    for (int j = 0; j < slots; ++j) {
+      const int e = __shfl_sync(0xffffffffu, e_j, j), pos = __shfl_sync(0xffffffffu, pos_j, j);
+      const float gs = __ldg(a.gs_a1 + e);
+      if (gs != gs_done) {
+        sb = quant_block16(v, gs, __fmul_rn(6.0f, gs), w0, w1);
+        gs_done = gs;
+      }
+      uint8_t* row = a.send + static_cast<int64_t>(pos) * a.row_bytes;
+      *reinterpret_cast<uint2*>(row + b * 8) = make_uint2(w0, w1);
+      row[a.H / 2 + b] = static_cast<uint8_t>(sb);
+    }
+  }
+}
+
 // Exclusive prefix sum over the 256 threads of the block (warp shuffles, then
 // the warps' totals); *total gets the sum.  Every thread must call it.
 __device__ __forceinline__ int32_t block_scan_excl(int32_t v, int32_t* warp_sums, int32_t* total) {
@@ -236,6 +323,14 @@ size_t ep_row_bytes(int H) { return (static_cast<size_t>(H) / 2 + static_cast<si
 cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s) {
   if (a.G > kEpMaxRanks) return cudaErrorInvalidValue;
   const int64_t R = static_cast<int64_t>(a.T) * a.k + (a.shared ? a.T : 0);
+  if (a.T > 256) {
+    ep_dispatch_place_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ep_dispatch_token_kernel<<<static_cast<unsigned>((a.T + kDispatchTokWarps - 1) / kDispatchTokWarps),
+                               kDispatchTokWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t blocks = R > 0 ? (R + 3) / 4 : 1;     // one CTA at least: it writes send_counts
   ep_dispatch_kernel<<<static_cast<unsigned>(blocks), 128, 0, s>>>(a);
   return cudaGetLastError();
