@@ -30,6 +30,7 @@
 #include "ptx.cuh"
 #include "quant_block.cuh"
 
+#include <algorithm>
 #include <cuda_bf16.h>
 
 namespace nvf {
@@ -210,16 +211,16 @@ __device__ __forceinline__ int32_t block_scan_excl(int32_t v, int32_t* warp_sums
   return base + x - v;
 }
 
-// One CTA of 256 threads: local offsets, tile offsets and, per (source s, local
-// expert j) cell c = s * J + j, the cell's first received row (recv_base) and
-// first grouped row (grp_base).  J = El + 1 count columns; Et_l = El + shared
-// local experts.  Thread t handles a contiguous chunk of experts, then of cells.
-__global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __restrict__ counts, int G, int El,
-                                                              int shared, int32_t* local_offsets,
-                                                              int32_t* local_tile_offsets, int32_t* recv_base,
-                                                              int32_t* grp_base) {
+// The receive plan, computed by one whole CTA: local offsets, tile offsets
+// and, per (source s, local expert j) cell c = s * J + j, the cell's first
+// received row (recv_base) and first grouped row (grp_base).  J = El + 1 count
+// columns; Et_l = El + shared local experts.  Thread t handles a contiguous
+// chunk of experts, then of cells.  The outputs may be in global or shared
+// memory; warp_sums is 32 ints of shared memory.
+__device__ void receive_plan(const int32_t* __restrict__ counts, int G, int El, int shared, int32_t* local_offsets,
+                             int32_t* local_tile_offsets, int32_t* recv_base, int32_t* grp_base,
+                             int32_t* warp_sums) {
   const int J = El + 1, Et_l = El + shared, cells = G * J;
-  __shared__ int32_t warp_sums[32];
   // experts [j0, j1) of this thread: totals over the sources, then the prefix
   const int per_e = (J + blockDim.x - 1) / blockDim.x;
   const int j0 = min(J, static_cast<int>(threadIdx.x) * per_e), j1 = min(J, j0 + per_e);
@@ -268,41 +269,87 @@ __global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __r
   }
 }
 
-// One warp per received row, 4 rows a CTA.
-__global__ void __launch_bounds__(128) ep_receive_scatter_kernel(const uint8_t* __restrict__ recv, int64_t n_recv,
-                                                                 int row_bytes, int H, int G, int El,
-                                                                 const int32_t* __restrict__ local_offsets,
-                                                                 const int32_t* __restrict__ local_tile_offsets,
-                                                                 const int32_t* __restrict__ recv_base,
-                                                                 const int32_t* __restrict__ grp_base,
-                                                                 const int32_t* __restrict__ counts, uint8_t* a1,
-                                                                 int32_t* recv_to_grp, int32_t* grp_to_recv,
-                                                                 int* err) {
-  const int lane = threadIdx.x & 31;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  if (i >= n_recv) return;
-  const int J = El + 1;
-  const int c = upper_group(recv_base, G * J, i);      // the (source, expert) cell holding row i
-  if (i - __ldg(recv_base + c) >= __ldg(counts + c)) {  // more rows than the counts hold: stay in bounds
-    if (lane == 0) report_error(err, DEV_BAD_OFFSETS, static_cast<int>(i));
-    return;
+// The plan alone (one CTA of 256 threads), for plans too large for the scatter
+// kernel's shared memory.
+__global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __restrict__ counts, int G, int El,
+                                                              int shared, int32_t* local_offsets,
+                                                              int32_t* local_tile_offsets, int32_t* recv_base,
+                                                              int32_t* grp_base) {
+  __shared__ int32_t warp_sums[32];
+  receive_plan(counts, G, El, shared, local_offsets, local_tile_offsets, recv_base, grp_base, warp_sums);
+}
+
+// One warp per received row, `rows` rows a CTA of 8 warps.  With PLAN (small
+// receives: a few hundred CTAs at most) every CTA first computes the receive
+// plan itself into shared memory -- a separate single-CTA plan kernel ahead of
+// the scatter cost a few microseconds of latency -- and CTA 0 writes the local
+// offsets out; otherwise (large receives, where thousands of CTAs would each
+// redo the plan) the plan comes from ep_receive_plan_kernel and the CTAs take
+// more rows each.  Either way the binary search for a row's (source, expert)
+// cell runs over cell starts in shared memory, not along a chain of dependent
+// global loads.
+constexpr int kScatterWarps = 8, kScatterPlanCells = 4096;
+constexpr int kScatterRowsSmall = 8, kScatterRowsLarge = 64, kScatterFusedMaxRows = 4096;
+template <bool PLAN>
+__global__ void __launch_bounds__(kScatterWarps * 32) ep_receive_scatter_kernel(
+    const uint8_t* __restrict__ recv, int64_t n_recv, int row_bytes, int H, int G, int El, int shared,
+    int32_t* local_offsets, int32_t* local_tile_offsets, const int32_t* __restrict__ recv_base_g,
+    const int32_t* __restrict__ grp_base_g, const int32_t* __restrict__ counts, uint8_t* a1, int32_t* recv_to_grp,
+    int32_t* grp_to_recv, int* err, int rows) {
+  extern __shared__ int32_t s_plan[];
+  __shared__ int32_t warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int J = El + 1, cells = G * J, Et_l = El + shared;
+  int32_t* s_rb = s_plan;                                // [cells]
+  int32_t* s_gb = s_plan + cells;                        // [cells] (PLAN)
+  int32_t* s_lo = s_plan + 2 * cells;                    // [Et_l + 1] (PLAN)
+  int32_t* s_lt = s_lo + Et_l + 1;                       // [Et_l + 1] (PLAN)
+  const int32_t* gb = grp_base_g;
+  const int32_t* lo = local_offsets;
+  const int32_t* lt = local_tile_offsets;
+  if constexpr (PLAN) {
+    receive_plan(counts, G, El, shared, s_lo, s_lt, s_rb, s_gb, warp_sums);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int j = threadIdx.x; j <= Et_l; j += blockDim.x) {
+        local_offsets[j] = s_lo[j];
+        local_tile_offsets[j] = s_lt[j];
+      }
+    gb = s_gb;
+    lo = s_lo;
+    lt = s_lt;
+  } else {
+    for (int c = threadIdx.x; c < cells; c += blockDim.x) s_rb[c] = __ldg(recv_base_g + c);
+    __syncthreads();
   }
-  const int j = c % J;
-  const int32_t g = __ldg(grp_base + c) + static_cast<int32_t>(i - __ldg(recv_base + c));
-  const int32_t local = g - __ldg(local_offsets + j);
-  const int64_t tile = __ldg(local_tile_offsets + j) + (local >> 7);
-  const uint32_t r = static_cast<uint32_t>(local & 127);
-  if (lane == 0) {
-    recv_to_grp[i] = g;
-    if (grp_to_recv != nullptr) grp_to_recv[g] = static_cast<int32_t>(i);
-  }
-  const uint8_t* row = recv + i * static_cast<int64_t>(row_bytes);
-  for (int gg = lane; gg < H / 64; gg += 32) {
-    const uint4 u0 = *reinterpret_cast<const uint4*>(row + gg * 32);
-    const uint4 u1 = *reinterpret_cast<const uint4*>(row + gg * 32 + 16);
-    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    const uint32_t sf = *reinterpret_cast<const uint32_t*>(row + H / 2 + gg * 4);
-    store_group64(a1, nullptr, LAYOUT_TILED_GROUPED, H, g, tile, r, gg, w, sf);
+  const bool a1_32 = (reinterpret_cast<uintptr_t>(a1) & 31u) == 0;
+  for (int m = warp; m < rows; m += kScatterWarps) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * rows + m;
+    if (i >= n_recv) break;
+    const int c = upper_group(s_rb, cells, i);         // the (source, expert) cell holding row i
+    if (i - s_rb[c] >= __ldg(counts + c)) {            // more rows than the counts hold: stay in bounds
+      if (lane == 0) report_error(err, DEV_BAD_OFFSETS, static_cast<int>(i));
+      continue;
+    }
+    const int j = c % J;
+    const int32_t g = gb[c] + static_cast<int32_t>(i - s_rb[c]);
+    const int32_t local = g - lo[j];
+    const int64_t tile = lt[j] + (local >> 7);
+    const uint32_t r = static_cast<uint32_t>(local & 127);
+    if (lane == 0) {
+      recv_to_grp[i] = g;
+      if (grp_to_recv != nullptr) grp_to_recv[g] = static_cast<int32_t>(i);
+    }
+    const uint8_t* row = recv + i * static_cast<int64_t>(row_bytes);
+    for (int gg = lane; gg < H / 64; gg += 32) {
+      const uint4 u0 = *reinterpret_cast<const uint4*>(row + gg * 32);
+      const uint4 u1 = *reinterpret_cast<const uint4*>(row + gg * 32 + 16);
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      const uint32_t sf = *reinterpret_cast<const uint32_t*>(row + H / 2 + gg * 4);
+      // one 32-byte store for the codes when a1 is 32-byte aligned (chunks are 18432 bytes)
+      if (a1_32) store_group64_tg32(a1, H, tile, r, gg, w, sf);
+      else store_group64(a1, nullptr, LAYOUT_TILED_GROUPED, H, g, tile, r, gg, w, sf);
+    }
   }
 }
 
@@ -342,13 +389,32 @@ cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes
                               int32_t* scratch, int* err, cudaStream_t s) {
   int32_t* recv_base = scratch;
   int32_t* grp_base = scratch + static_cast<int64_t>(G) * (El + 1);
+  const int cells = G * (El + 1), Et_l = El + shared;
+  if (cells <= kScatterPlanCells && n_recv <= kScatterFusedMaxRows) {
+    const int rows = kScatterRowsSmall;
+    const unsigned blocks = static_cast<unsigned>(std::max<int64_t>((n_recv + rows - 1) / rows, 1));
+    // plan and scatter in one kernel (at least one CTA: it writes the local offsets)
+    const size_t smem = static_cast<size_t>(2 * cells + 2 * (Et_l + 1)) * 4;
+    ep_receive_scatter_kernel<true><<<blocks, kScatterWarps * 32, smem, s>>>(
+        recv, n_recv, row_bytes, H, G, El, shared, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
+        recv_to_grp, grp_to_recv, err, rows);
+    return cudaGetLastError();
+  }
   ep_receive_plan_kernel<<<1, 256, 0, s>>>(counts, G, El, shared, local_offsets, local_tile_offsets, recv_base,
                                             grp_base);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || n_recv == 0) return e;
-  ep_receive_scatter_kernel<<<static_cast<unsigned>((n_recv + 3) / 4), 128, 0, s>>>(
-      recv, n_recv, row_bytes, H, G, El, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
-      recv_to_grp, grp_to_recv, err);
+  const size_t smem = static_cast<size_t>(cells) * 4;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(ep_receive_scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const int rows = kScatterRowsLarge;
+  const unsigned blocks = static_cast<unsigned>((n_recv + rows - 1) / rows);
+  ep_receive_scatter_kernel<false><<<blocks, kScatterWarps * 32, smem, s>>>(
+      recv, n_recv, row_bytes, H, G, El, shared, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
+      recv_to_grp, grp_to_recv, err, rows);
   return cudaGetLastError();
 }
 

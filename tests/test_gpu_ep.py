@@ -125,12 +125,14 @@ def test_layer_matches_single_device(nvf, G, shared, Ts):
 
 
 # Above 256 tokens a rank's dispatch runs token by token (a place pass, then a
-# quantize-and-store pass): 300 and 260 tokens take that path.
+# quantize-and-store pass): 300 and 260 tokens take that path.  Up to 4096
+# received rows the receive plans inside the scatter kernel; the two ranks of
+# 1200 + 1100 tokens receive ~4600 rows each, past that.
 @pytest.mark.parametrize("shared,Ts", [(False, [9, 70, 0, 31]), (True, [9, 70, 0, 31]), (True, [300, 5, 260, 0]),
-                                       (False, [300, 5, 260, 0])])
+                                       (False, [300, 5, 260, 0]), (True, [1200, 1100])])
 def test_dispatch_and_receive_match_the_oracle(nvf, shared, Ts):
     cfg = CONFIGS["tiny"].scaled(E=16, k=4, shared=shared, name="tiny_ep")
-    G = 4
+    G = len(Ts)
     ranks = EmulatedRanks(nvf, cfg, G, Ts, seed=5)
     El, H = cfg.E // G, cfg.H
     plans = []
