@@ -510,10 +510,13 @@ static nvf_status forward_impl(const nvf_moe_weights* w, const void* w_gate, int
   ra.gs_a1 = gs_a1;
   ra.a1 = base + L.a1;
   ra.tile_group = i32(L.tile_group);
-  // Kernels after the first start while their predecessor drains (programmatic
-  // dependent launch), unless stage boundaries are being timed: an event
-  // between two kernels is a full dependency.
+  // Every kernel starts while its predecessor drains (programmatic dependent
+  // launch), unless stage boundaries are being timed: an event between two
+  // kernels is a full dependency.  The first routing kernel too: it waits for
+  // whatever ran before it on the stream (griddepcontrol.wait) before it reads
+  // anything, and the kernels after it start only once it has passed that wait.
   const bool pdl = stage_events == nullptr;
+  ra.pdl = pdl;
   NVF_CUDA(launch_route(ra, s), "route launch");
   NVF_CUDA(mark(1), "cudaEventRecord");
 
