@@ -21,13 +21,16 @@ def nvf():
     return m
 
 
-@pytest.mark.parametrize("shared,out_dtype", [(False, torch.bfloat16), (True, torch.float32)])
-def test_graph_step_equals_the_separate_calls(nvf, shared, out_dtype):
+@pytest.mark.parametrize("shared,out_dtype,with_bias", [(False, torch.bfloat16, False), (True, torch.float32, False),
+                                                        (False, torch.bfloat16, True)])
+def test_graph_step_equals_the_separate_calls(nvf, shared, out_dtype, with_bias):
     cfg = CONFIGS["tiny"].scaled(T=24, shared=shared, name="tiny_graph")
     w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, shared, lambda e: expert_weights(cfg, e, 0))
     gs_a1 = torch.full((cfg.E_total,), 0.0012672061566263437, device="cuda")
     gs_a2 = torch.full((cfg.E_total,), 0.00016923830844461918, device="cuda")
-    g = nvf.MoEGraph(w, cfg.T, cfg.k, gs_a1, gs_a2, out_dtype=out_dtype)
+    # a selection bias that changes which experts win
+    bias = torch.linspace(-1.0, 1.0, cfg.E, device="cuda") if with_bias else None
+    g = nvf.MoEGraph(w, cfg.T, cfg.k, gs_a1, gs_a2, bias=bias, out_dtype=out_dtype)
     for seed in (0, 1):                      # the second launch sees new host inputs
         x, lg, _ = make_inputs(cfg, seed)
         g.x.copy_(x)
@@ -36,7 +39,7 @@ def test_graph_step_equals_the_separate_calls(nvf, shared, out_dtype):
         torch.cuda.synchronize()
         code, detail = nvf.device_status()
         assert code == 0, (code, detail)
-        ref = nvf.moe_forward(w, x.cuda(), lg.cuda(), cfg.k, gs_a1, gs_a2, out_dtype=out_dtype)
+        ref = nvf.moe_forward(w, x.cuda(), lg.cuda(), cfg.k, gs_a1, gs_a2, bias=bias, out_dtype=out_dtype)
         assert torch.equal(g.out, ref.cpu()), seed
     g.close()
 

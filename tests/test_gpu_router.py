@@ -44,7 +44,7 @@ def _check_logits(got, xb, wb):
 # three 256-row blocks, the last with 16.
 @pytest.mark.parametrize("T,H,n", [(1, 256, 8), (37, 2048, 129), (64, 128, 9), (65, 256, 33), (128, 256, 33),
                                    (300, 2048, 128), (4096, 2048, 129), (256, 4096, 513), (6000, 512, 40),
-                                   (10000, 256, 33)])
+                                   (10000, 256, 33), (100, 256, 1)])
 def test_router_gemm_matches_the_oracle(nvf, T, H, n):
     g = torch.Generator().manual_seed(T + H + n)
     x = torch.randn(T, H, generator=g).to(torch.bfloat16)
