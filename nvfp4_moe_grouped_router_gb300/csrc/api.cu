@@ -180,17 +180,20 @@ namespace nvf {
 // ~8 us to the layer; two copy-engine copies added ~17 us.
 __global__ void __launch_bounds__(256) graph_copy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                                                          size_t n) {
+  // launched behind the layer's last kernel, it reads that kernel's output only
+  // after it has finished; the layer's first kernel may launch meanwhile
+  griddep_wait();
+  griddep_launch_dependents();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x, n16 = n / 16;
   for (size_t j = i0; j < n16; j += stride) reinterpret_cast<uint4*>(dst)[j] = reinterpret_cast<const uint4*>(src)[j];
   for (size_t j = n16 * 16 + i0; j < n; j += stride) dst[j] = src[j];
 }
-cudaError_t copy_bytes(void* dst, const void* src, size_t n, cudaStream_t s) {
+cudaError_t copy_bytes(void* dst, const void* src, size_t n, cudaStream_t s, bool pdl) {
   const size_t n16 = (n + 15) / 16;
   const int blocks = static_cast<int>(std::min<size_t>((n16 + 255) / 256, static_cast<size_t>(4 * sm_count())));
-  graph_copy_kernel<<<std::max(blocks, 1), 256, 0, s>>>(static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src),
-                                                        n);
-  return cudaGetLastError();
+  return launch_kernel(graph_copy_kernel, dim3(std::max(blocks, 1)), dim3(256), 0, s, pdl,
+                       static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src), n);
 }
 
 // One CTA waits on an mbarrier that nothing arrives on, through the pipeline's
@@ -819,16 +822,16 @@ nvf_status nvf_moe_graph_create(const nvf_moe_weights* w, int32_t T, int32_t k, 
   // the inputs (one copy when logits_host directly follows x_host, as on the
   // device), then the layer, then the result back
   if (static_cast<const uint8_t*>(ld) == static_cast<const uint8_t*>(xd) + xb) {
-    e = copy_bytes(g->x, xd, xb + lb, g->stream);
+    e = copy_bytes(g->x, xd, xb + lb, g->stream, false);
   } else {
-    e = copy_bytes(g->x, xd, xb, g->stream);
-    if (e == cudaSuccess) e = copy_bytes(g->logits, ld, lb, g->stream);
+    e = copy_bytes(g->x, xd, xb, g->stream, false);
+    if (e == cudaSuccess) e = copy_bytes(g->logits, ld, lb, g->stream, true);
   }
   nvf_status st = NVF_OK;
   if (e == cudaSuccess)
     st = forward_impl(w, nullptr, 0, g->x, g->logits, bias, T, k, renormalize, gs_a1, gs_a2, out_dtype, g->out,
                       nullptr, g->ws, L.total, nullptr, g->stream);
-  if (e == cudaSuccess && st == NVF_OK) e = copy_bytes(od, g->out, ob, g->stream);
+  if (e == cudaSuccess && st == NVF_OK) e = copy_bytes(od, g->out, ob, g->stream, true);
   const cudaError_t ec = cudaStreamEndCapture(g->stream, &g->graph);
   if (st != NVF_OK) return bail(st);                     // the forward's own message stands
   if (e != cudaSuccess) return bail(cuda_fail(e, "graph capture"));

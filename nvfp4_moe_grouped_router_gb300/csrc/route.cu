@@ -445,6 +445,10 @@ __global__ void __launch_bounds__(256, BF16 ? 4 : 2) combine_kernel(const void* 
     }
   }
   griddep_wait();
+  // A decode batch: the next kernel may launch now (it waits for this grid to
+  // finish before it reads anything).  A large batch keeps the SMs to itself:
+  // an early launch there parks the next kernel's CTAs on them (prefill +3 us).
+  if (T <= 256) griddep_launch_dependents();
   if (!live) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   {
