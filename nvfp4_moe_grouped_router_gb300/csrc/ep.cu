@@ -104,13 +104,16 @@ __global__ void __launch_bounds__(128) ep_dispatch_kernel(EpDispatchArgs a) {
 // writes the row.
 __global__ void __launch_bounds__(256) ep_dispatch_place_kernel(EpDispatchArgs a) {
   __shared__ int64_t send_off[kEpMaxRanks + 1];
+  extern __shared__ int32_t s_offsets[];                 // [Et + 1]: the binary search runs here
   const int El = a.E / a.G, Et = a.E + a.shared;
+  for (int e = threadIdx.x; e <= Et; e += blockDim.x) s_offsets[e] = __ldg(a.offsets + e);
+  __syncthreads();
   if (threadIdx.x == 0) {
     int64_t acc = 0;
     for (int r = 0; r < a.G; ++r) {
       send_off[r] = acc;
-      acc += __ldg(a.offsets + (r + 1) * El) - __ldg(a.offsets + r * El);
-      if (r == a.rank && a.shared) acc += __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+      acc += s_offsets[(r + 1) * El] - s_offsets[r * El];
+      if (r == a.rank && a.shared) acc += s_offsets[a.E + 1] - s_offsets[a.E];
     }
     send_off[a.G] = acc;
   }
@@ -118,23 +121,23 @@ __global__ void __launch_bounds__(256) ep_dispatch_place_kernel(EpDispatchArgs a
     for (int c = threadIdx.x; c < a.G * (El + 1); c += blockDim.x) {
       const int r = c / (El + 1), j = c - r * (El + 1);
       int n = 0;
-      if (j < El) n = __ldg(a.offsets + r * El + j + 1) - __ldg(a.offsets + r * El + j);
-      else if (r == a.rank && a.shared) n = __ldg(a.offsets + a.E + 1) - __ldg(a.offsets + a.E);
+      if (j < El) n = s_offsets[r * El + j + 1] - s_offsets[r * El + j];
+      else if (r == a.rank && a.shared) n = s_offsets[a.E + 1] - s_offsets[a.E];
       a.send_counts[c] = n;
     }
   }
   __syncthreads();
   const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t R = __ldg(a.offsets + Et);
+  const int64_t R = s_offsets[Et];
   if (p >= R) return;
-  const int e = upper_group(a.offsets, Et, p);
+  const int e = upper_group(s_offsets, Et, p);
   int64_t pos;
   if (e < a.E) {
     const int dest = e / El;
-    pos = send_off[dest] + (p - __ldg(a.offsets + dest * El));
+    pos = send_off[dest] + (p - s_offsets[dest * El]);
   } else {
-    const int64_t own_routed = __ldg(a.offsets + (a.rank + 1) * El) - __ldg(a.offsets + a.rank * El);
-    pos = send_off[a.rank] + own_routed + (p - __ldg(a.offsets + a.E));
+    const int64_t own_routed = s_offsets[(a.rank + 1) * El] - s_offsets[a.rank * El];
+    pos = send_off[a.rank] + own_routed + (p - s_offsets[a.E]);
   }
   a.src_to_send[__ldg(a.perm_to_src + p)] = static_cast<int32_t>(pos);
   *reinterpret_cast<int32_t*>(a.send + pos * static_cast<int64_t>(a.row_bytes)) = e;
@@ -279,15 +282,15 @@ __global__ void __launch_bounds__(256) ep_receive_plan_kernel(const int32_t* __r
   receive_plan(counts, G, El, shared, local_offsets, local_tile_offsets, recv_base, grp_base, warp_sums);
 }
 
-// One warp per received row, `rows` rows a CTA of 8 warps.  With PLAN (small
-// receives: a few hundred CTAs at most) every CTA first computes the receive
-// plan itself into shared memory -- a separate single-CTA plan kernel ahead of
-// the scatter cost a few microseconds of latency -- and CTA 0 writes the local
-// offsets out; otherwise (large receives, where thousands of CTAs would each
-// redo the plan) the plan comes from ep_receive_plan_kernel and the CTAs take
-// more rows each.  Either way the binary search for a row's (source, expert)
-// cell runs over cell starts in shared memory, not along a chain of dependent
-// global loads.
+// One warp per received row, `rows` rows a CTA of 8 warps (8 up to 4096
+// received rows, 64 above, so that large receives do not run thousands of
+// CTAs).  With PLAN (G * (El + 1) <= kScatterPlanCells) every CTA first
+// computes the receive plan itself into shared memory -- a separate
+// single-CTA plan kernel ahead of the scatter cost ~5 us of latency -- and
+// CTA 0 writes the local offsets out; otherwise the plan comes from
+// ep_receive_plan_kernel.  Either way the binary search for a row's (source,
+// expert) cell runs over cell starts in shared memory, not along a chain of
+// dependent global loads.
 constexpr int kScatterWarps = 8, kScatterPlanCells = 4096;
 constexpr int kScatterRowsSmall = 8, kScatterRowsLarge = 64, kScatterFusedMaxRows = 4096;
 template <bool PLAN>
@@ -371,7 +374,8 @@ cudaError_t launch_ep_dispatch(const EpDispatchArgs& a, cudaStream_t s) {
   if (a.G > kEpMaxRanks) return cudaErrorInvalidValue;
   const int64_t R = static_cast<int64_t>(a.T) * a.k + (a.shared ? a.T : 0);
   if (a.T > 256) {
-    ep_dispatch_place_kernel<<<static_cast<unsigned>((R + 255) / 256), 256, 0, s>>>(a);
+    ep_dispatch_place_kernel<<<static_cast<unsigned>((R + 255) / 256), 256,
+                               static_cast<size_t>(a.E + a.shared + 1) * sizeof(int32_t), s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ep_dispatch_token_kernel<<<static_cast<unsigned>((a.T + kDispatchTokWarps - 1) / kDispatchTokWarps),
@@ -390,8 +394,8 @@ cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes
   int32_t* recv_base = scratch;
   int32_t* grp_base = scratch + static_cast<int64_t>(G) * (El + 1);
   const int cells = G * (El + 1), Et_l = El + shared;
-  if (cells <= kScatterPlanCells && n_recv <= kScatterFusedMaxRows) {
-    const int rows = kScatterRowsSmall;
+  if (cells <= kScatterPlanCells) {
+    const int rows = n_recv <= kScatterFusedMaxRows ? kScatterRowsSmall : kScatterRowsLarge;
     const unsigned blocks = static_cast<unsigned>(std::max<int64_t>((n_recv + rows - 1) / rows, 1));
     // plan and scatter in one kernel (at least one CTA: it writes the local offsets)
     const size_t smem = static_cast<size_t>(2 * cells + 2 * (Et_l + 1)) * 4;
@@ -410,7 +414,7 @@ cudaError_t launch_ep_receive(const uint8_t* recv, int64_t n_recv, int row_bytes
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  const int rows = kScatterRowsLarge;
+  const int rows = n_recv <= kScatterFusedMaxRows ? kScatterRowsSmall : kScatterRowsLarge;
   const unsigned blocks = static_cast<unsigned>((n_recv + rows - 1) / rows);
   ep_receive_scatter_kernel<false><<<blocks, kScatterWarps * 32, smem, s>>>(
       recv, n_recv, row_bytes, H, G, El, shared, local_offsets, local_tile_offsets, recv_base, grp_base, counts, a1,
