@@ -443,7 +443,9 @@ size_t nvf_ep_receive_scratch_words(int32_t G, int32_t El);
  * [El + shared + 1] (local expert j's rows: source 0's, then source 1's, ...);
  * recv_to_grp int32 [n_recv], received row i's grouped row; grp_to_recv
  * (nullable) int32 [n_recv], its inverse.  scratch: device int32
- * [nvf_ep_receive_scratch_words(G, El)]. */
+ * [nvf_ep_receive_scratch_words(G, El)].  Limits: 1 <= G <= 1024, El >= 1,
+ * G * (El + 1) <= 57344 (the per-cell table is kept in shared memory);
+ * otherwise NVF_ERR_INVALID_ARG. */
 nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* recv_counts, int32_t G, int32_t El,
                           int32_t shared, int32_t H, uint8_t* a1, int32_t* local_offsets,
                           int32_t* local_tile_offsets, int32_t* recv_to_grp, int32_t* grp_to_recv, int32_t* scratch,

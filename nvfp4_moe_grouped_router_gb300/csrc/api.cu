@@ -655,6 +655,8 @@ nvf_status nvf_ep_receive(const void* recv_rows, int64_t n_recv, const int32_t* 
   NVF_BEGIN();
   NVF_REQUIRE(G >= 1 && G <= 1024 && El >= 1 && (shared == 0 || shared == 1), "G=%d, El=%d, shared=%d out of range",
               G, El, shared);
+  NVF_REQUIRE(static_cast<int64_t>(G) * (El + 1) <= 57344, "G * (El + 1) = %lld exceeds 57344",
+              static_cast<long long>(G) * (El + 1));
   NVF_REQUIRE(H > 0 && H % 128 == 0, "H=%d must be a positive multiple of 128", H);
   NVF_REQUIRE(n_recv >= 0 && n_recv < (int64_t(1) << 31), "n_recv=%lld out of range", (long long)n_recv);
   NVF_REQUIRE(recv_counts && local_offsets && local_tile_offsets && scratch,

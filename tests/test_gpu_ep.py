@@ -196,3 +196,33 @@ def test_argument_validation(nvf):
         nvf.ep_dispatch(x.cuda(), route, cfg.E, cfg.k, False, 3, 0, g)
     with pytest.raises(nvf.NvfError, match="rank"):
         nvf.ep_dispatch(x.cuda(), route, cfg.E, cfg.k, False, 4, 4, g)
+
+
+@pytest.mark.parametrize("G,El,shared", [(2, 2100, True), (3, 40, False)])
+def test_receive_many_cells(nvf, G, El, shared):
+    """A receive over many (source, expert) cells, most of them empty: past 4096
+    cells the plan comes from its own kernel (2 x 2101 cells), else from the
+    scatter kernel.  Rows are arbitrary bytes: the receive only moves them."""
+    H = 256
+    rng = np.random.default_rng(G * 1000 + El)
+    J = El + 1
+    counts = np.zeros((G, J), np.int32)
+    nz = rng.choice(G * J, size=min(60, G * J), replace=False)
+    counts.reshape(-1)[nz] = rng.integers(1, 4, size=nz.size)
+    if not shared:
+        counts[:, El] = 0
+    n = int(counts.sum())
+    row_bytes = nvf.ep_row_bytes(H)
+    rows = rng.integers(0, 256, size=(n, row_bytes), dtype=np.uint8)
+    g = nvf.ep_receive(torch.from_numpy(rows).cuda(), torch.from_numpy(counts).cuda(), El, shared, H, n)
+    code, detail = nvf.device_status()
+    assert code == 0, (code, detail)
+    off, r2g = EP.receive_order(counts)
+    Et = El + int(shared)
+    assert np.array_equal(g["offsets"].cpu().numpy(), off[:Et + 1])
+    assert np.array_equal(g["recv_to_grp"].cpu().numpy(), r2g)
+    assert np.array_equal(g["tile_offsets"].cpu().numpy(), M.tile_offsets(np.diff(off[:Et + 1])))
+    tile, rr = row_tiles(n, off[:Et + 1], g["tile_offsets"].cpu().numpy())
+    codes, scales = tiled_unpack(g["a1"].cpu().numpy(), H, tile, rr)
+    assert np.array_equal(codes[r2g], rows[:, :H // 2])
+    assert np.array_equal(scales[r2g], rows[:, H // 2:H // 2 + H // 16])
