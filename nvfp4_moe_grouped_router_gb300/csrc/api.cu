@@ -177,7 +177,7 @@ namespace nvf {
 // Host <-> device copy done by the SMs over the device's mapping of page-locked
 // host memory (16-byte pieces, grid-stride; dst and src 16-byte aligned).  In
 // the captured decode step (147 KB in, 131 KB out) the two copy kernels add
-// ~8 us to the layer; two copy-engine copies added ~17 us.
+// ~6 us to the layer; two copy-engine copies added ~17 us.
 __global__ void __launch_bounds__(256) graph_copy_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                                                          size_t n) {
   // launched behind the layer's last kernel, it reads that kernel's output only
