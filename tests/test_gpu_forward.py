@@ -254,6 +254,15 @@ def test_tiny_layer(nvf):
     check_layer(nvf, layer, torch.bfloat16)
 
 
+@pytest.mark.parametrize("k,shared,T", [(1, False, 16), (8, False, 16), (8, True, 40), (2, True, 100)])
+def test_routing_extremes(nvf, k, shared, T):
+    """Top-1, top-E (every expert on every token), a shared expert beside
+    top-E, and a batch between the small-group (<= 32 rows) and the
+    large-batch (> 256 tokens) paths: the whole layer against the oracle."""
+    cfg = CONFIGS["tiny"].scaled(k=k, shared=shared, T=T, name=f"tiny_k{k}_s{int(shared)}_t{T}")
+    check_layer(nvf, Layer(nvf, cfg, parent="tiny"), torch.float32)
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_decode_layer(nvf, out_dtype):
     check_layer(nvf, Layer(nvf, CONFIGS["decode"]), out_dtype)
