@@ -21,10 +21,12 @@ def nvf():
     return m
 
 
-@pytest.mark.parametrize("shared,out_dtype,with_bias", [(False, torch.bfloat16, False), (True, torch.float32, False),
-                                                        (False, torch.bfloat16, True)])
-def test_graph_step_equals_the_separate_calls(nvf, shared, out_dtype, with_bias):
-    cfg = CONFIGS["tiny"].scaled(T=24, shared=shared, name="tiny_graph")
+@pytest.mark.parametrize("shared,out_dtype,with_bias,T", [(False, torch.bfloat16, False, 24),
+                                                          (True, torch.float32, False, 24),
+                                                          (False, torch.bfloat16, True, 24),
+                                                          (True, torch.bfloat16, False, 300)])
+def test_graph_step_equals_the_separate_calls(nvf, shared, out_dtype, with_bias, T):
+    cfg = CONFIGS["tiny"].scaled(T=T, shared=shared, name="tiny_graph")
     w = nvf.prepare_weights(cfg.E, cfg.H, cfg.I, shared, lambda e: expert_weights(cfg, e, 0))
     gs_a1 = torch.full((cfg.E_total,), 0.0012672061566263437, device="cuda")
     gs_a2 = torch.full((cfg.E_total,), 0.00016923830844461918, device="cuda")
