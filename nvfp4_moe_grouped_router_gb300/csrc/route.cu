@@ -46,7 +46,7 @@ namespace {
 constexpr int kMaxE = 1024;          // routed experts
 constexpr int kInlineWords = 8;      // up to 256 tokens the permute kernel counts bits itself
 constexpr int kPermWarps = 16;       // tokens per permute CTA (up to 256 tokens)
-constexpr int kPermTokWarps = 8;     // tokens per permute CTA (more than 256 tokens: up to 4 CTAs a SM)
+constexpr int kPermTokWarps = 4;     // tokens per permute CTA (more than 256 tokens: up to 8 CTAs a SM)
 constexpr int kCombineSlots = 8;     // the combine keeps up to this many slots in flight per thread
 
 template <int NV>
@@ -297,7 +297,7 @@ __device__ __forceinline__ uint32_t quant_packed64(const uint4 (&xr)[8], float g
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kPermTokWarps * 32, 4) route_permute_kernel(RouteArgs a, int W) {
+__global__ void __launch_bounds__(kPermTokWarps * 32, 8) route_permute_kernel(RouteArgs a, int W) {
   __shared__ int offs[kMaxE + 2];
   __shared__ int til[kMaxE + 2];
   __shared__ int s_pos[MODE == PERM_TOKEN ? kPermTokWarps : 1][33];
