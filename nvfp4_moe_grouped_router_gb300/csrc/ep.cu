@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_place_kernel(EpDispatchArgs a
 // expert (every slot's before any lane writes a row), then each lane quantizes
 // its 16-element blocks of the token once per distinct global scale and writes
 // them to every slot's row.
-constexpr int kDispatchTokWarps = 8;
+constexpr int kDispatchTokWarps = 4;
 __global__ void __launch_bounds__(kDispatchTokWarps * 32) ep_dispatch_token_kernel(EpDispatchArgs a) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kDispatchTokWarps + (threadIdx.x >> 5);
